@@ -1,0 +1,277 @@
+"""CPU oracle for the DCP decode hot path.  TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never calls it.  It shares no code with the CUDA path:
+both sides see only the seeded inputs from the ``workloads`` module.
+
+Everything here is plain numpy, fp64 for floating point, written directly
+from the definitions on the pages it cites:
+
+* "Decode Context Parallel (DCP)" (docs.vllm.ai, vLLM Ascend design docs),
+  section "KV-cache layout": the four token -> (virtual block, offset, local
+  block, rank) formulas and the ``block_size % interleave == 0`` constraint;
+  section "Backend structure": the per-rank context-length matrix and the
+  partial-output / LSE merge; sections "Decode" and "GLM-5.2 SFA DCP
+  replicated indexer": attention over the local shard, and the remap of
+  global top-k indices to local KV indices.
+* "DeepSeek V4.1 context parallelism" (lightseek.org TokenSpeed design),
+  section "Cache ownership": writes translate virtual slots to local slots
+  and mask non-owners; section "Decode computation": the attention sink is
+  applied once when the partials are merged by log-sum-exp.
+
+Readings where the pages are silent (each listed in the design doc):
+
+* local in-block offset of token x on its rank:
+  ``loc = (local_block_index // dcp) * I + offset_in_virtual_block % I`` and
+  local position ``vb * block_size + loc``; the slot is
+  ``BT[rank][b][vb] * block_size + loc``;
+* LSE is the natural log of the sum of exp of the *scaled* scores;
+* an empty shard has ``lse = -inf`` and ``o = 0``;
+* the sink is one logit per query head, in scaled-score units, with a zero
+  value vector.
+
+Parity status: every function below is pinned by ``tests/test_oracle_pins.py``
+(brute-force enumeration, closed forms, library routines, invariants).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+NEG_INF = float("-inf")
+
+
+# ---------------------------------------------------------------------------
+# KV-cache layout ("Decode Context Parallel (DCP)", section "KV-cache layout")
+# ---------------------------------------------------------------------------
+
+def check_layout(dcp: int, bs: int, I: int) -> None:
+    """The page requires block_size % cp_kv_cache_interleave_size == 0."""
+    if dcp < 1 or bs < 1 or I < 1 or bs % I != 0:
+        raise ValueError(f"invalid DCP layout dcp={dcp} block_size={bs} interleave={I}")
+
+
+def virtual_block_index(x, bs, dcp):
+    return x // (bs * dcp)
+
+
+def offset_in_virtual_block(x, bs, dcp):
+    return x % (bs * dcp)
+
+
+def local_block_index(x, bs, dcp, I):
+    return offset_in_virtual_block(x, bs, dcp) // I
+
+
+def target_rank(x, bs, dcp, I):
+    return local_block_index(x, bs, dcp, I) % dcp
+
+
+def local_offset(x, bs, dcp, I):
+    """Offset of token x inside its rank's physical block (reading, see module doc)."""
+    return (local_block_index(x, bs, dcp, I) // dcp) * I + offset_in_virtual_block(x, bs, dcp) % I
+
+
+def local_position(x, bs, dcp, I):
+    """Position of token x in its rank's local sequence shard."""
+    return virtual_block_index(x, bs, dcp) * bs + local_offset(x, bs, dcp, I)
+
+
+def global_token(p, r, bs, dcp, I):
+    """Inverse of (target_rank, local_position): local position p on rank r -> token x."""
+    vb, loc = p // bs, p % bs
+    lbi = (loc // I) * dcp + r
+    return vb * bs * dcp + lbi * I + loc % I
+
+
+def local_seq_lens(seq_lens, dcp, bs, I) -> np.ndarray:
+    """Per-rank context-length matrix [B, dcp], counted by enumerating every token.
+
+    ("Backend structure": the DCP metadata owns the per-rank context-length matrix.)
+    """
+    check_layout(dcp, bs, I)
+    out = np.zeros((len(seq_lens), dcp), dtype=np.int64)
+    for b, L in enumerate(seq_lens):
+        x = np.arange(int(L), dtype=np.int64)
+        out[b] = np.bincount(target_rank(x, bs, dcp, I), minlength=dcp)
+    return out
+
+
+def local_seq_len_closed_form(L, r, dcp, bs, I):
+    """Closed form for the number of tokens x < L owned by rank r."""
+    full, rem = L // (bs * dcp), L % (bs * dcp)
+    c, p = rem // I, rem % I
+    return full * bs + (c // dcp) * I + (I if c % dcp > r else 0) + (p if c % dcp == r else 0)
+
+
+def slot_mapping(req, pos, block_table, seq_lens_unused, dcp, bs, I, num_blocks):
+    """Token -> (owner rank, per-rank slot with -1 on non-owners).
+
+    req[T], pos[T]: request index and global position of each token.
+    block_table[dcp][B][max_vb]: physical block of virtual block vb on rank r.
+    Invalid tokens (request out of range, pos < 0, virtual block beyond the
+    table, or a table entry outside [0, num_blocks)) get rank -1 and no slot.
+    ("KV-cache layout"; "Cache ownership": translate virtual slots to local
+    slots and mask non-owners.)
+    """
+    check_layout(dcp, bs, I)
+    req = np.asarray(req, dtype=np.int64)
+    pos = np.asarray(pos, dtype=np.int64)
+    T = len(req)
+    B, max_vb = block_table.shape[1], block_table.shape[2]
+    rank = np.full(T, -1, dtype=np.int64)
+    slot = np.full((dcp, T), -1, dtype=np.int64)
+    for t in range(T):
+        b, x = int(req[t]), int(pos[t])
+        if b < 0 or b >= B or x < 0:
+            continue
+        vb = virtual_block_index(x, bs, dcp)
+        if vb >= max_vb:
+            continue
+        r = target_rank(x, bs, dcp, I)
+        phys = int(block_table[r, b, vb])
+        if phys < 0 or phys >= num_blocks:
+            continue
+        rank[t] = r
+        slot[r, t] = phys * bs + local_offset(x, bs, dcp, I)
+    return rank, slot
+
+
+def sfa_remap(topk, seq_lens, block_table, dcp, bs, I, num_blocks):
+    """Global top-k token indices -> (rank, local slot); invalid entries -> (-1, -1).
+
+    ("GLM-5.2 SFA DCP replicated indexer": global indices from the replicated
+    indexer view are remapped to local KV indices before SFA runs.)
+    """
+    B, K = topk.shape
+    rank = np.full((B, K), -1, dtype=np.int64)
+    slot = np.full((B, K), -1, dtype=np.int64)
+    for b in range(B):
+        for k in range(K):
+            g = int(topk[b, k])
+            if g < 0 or g >= int(seq_lens[b]):
+                continue
+            vb = virtual_block_index(g, bs, dcp)
+            if vb >= block_table.shape[2]:
+                continue
+            r = target_rank(g, bs, dcp, I)
+            phys = int(block_table[r, b, vb])
+            if phys < 0 or phys >= num_blocks:
+                continue
+            rank[b, k] = r
+            slot[b, k] = phys * bs + local_offset(g, bs, dcp, I)
+    return rank, slot
+
+
+# ---------------------------------------------------------------------------
+# owner-masked paged cache ("Cache ownership")
+# ---------------------------------------------------------------------------
+
+def build_caches(rows, slot, dcp, num_blocks, bs, sentinel):
+    """Per-rank paged caches with token-major layout [num_blocks*bs, width].
+
+    rows[T, width]: one row per token (any dtype; copied bit for bit).
+    slot[dcp, T]: slot of token t on rank r or -1 (non-owner: not written).
+    Bytes never written keep ``sentinel``.
+    """
+    T, width = rows.shape
+    caches = np.full((dcp, num_blocks * bs, width), sentinel, dtype=rows.dtype)
+    for r in range(dcp):
+        for t in range(T):
+            s = int(slot[r, t])
+            if s >= 0:
+                caches[r, s] = rows[t]
+    return caches
+
+
+# ---------------------------------------------------------------------------
+# attention (fp64) and the exact LSE merge
+# ---------------------------------------------------------------------------
+
+def attention(q, K, V, scale):
+    """Softmax attention of one query over a set of keys, fp64.
+
+    q[dk], K[n, dk], V[n, dv] -> (o[dv], lse) with s_j = scale * q.k_j,
+    lse = ln sum_j exp(s_j), o = sum_j exp(s_j - lse) v_j.  n == 0 gives
+    (0, -inf).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    if K.shape[0] == 0:
+        return np.zeros(V.shape[1], dtype=np.float64), NEG_INF
+    s = scale * (K @ q)
+    m = s.max()
+    lse = m + math.log(np.exp(s - m).sum())
+    o = np.exp(s - lse) @ V
+    return o, lse
+
+
+def shard_tokens(L, r, dcp, bs, I):
+    """Global token ids owned by rank r among [0, L), in local-position order."""
+    n = local_seq_len_closed_form(L, r, dcp, bs, I)
+    return global_token(np.arange(n, dtype=np.int64), r, bs, dcp, I)
+
+
+def lse_merge(parts_o, parts_lse, sink=None):
+    """Exact merge of partial attention results by log-sum-exp.
+
+    parts_o[n, dv], parts_lse[n]; sink: optional logit added once to the
+    denominator with a zero value vector ("Decode computation" on the
+    TokenSpeed page).  Returns (o[dv], lse); all parts empty and no sink
+    gives (0, -inf).
+    """
+    parts_o = np.asarray(parts_o, dtype=np.float64)
+    lses = [float(x) for x in parts_lse]
+    if sink is not None:
+        lses_all = lses + [float(sink)]
+    else:
+        lses_all = lses
+    finite = [x for x in lses_all if x != NEG_INF]
+    if not finite:
+        return np.zeros(parts_o.shape[1], dtype=np.float64), NEG_INF
+    m = max(finite)
+    lse = m + math.log(sum(math.exp(x - m) for x in finite))
+    o = np.zeros(parts_o.shape[1], dtype=np.float64)
+    for i, x in enumerate(lses):
+        if x != NEG_INF:
+            o += math.exp(x - lse) * parts_o[i]
+    return o, lse
+
+
+def sharded_attention(q, K_all, V_all, scale, L, dcp, bs, I, sink=None):
+    """DCP decode for one (request, head): per-rank partials, then the merge.
+
+    K_all/V_all hold the request's keys/values in global token order.
+    Returns (o, lse, per_rank_o[dcp, dv], per_rank_lse[dcp]).
+    """
+    dv = V_all.shape[1]
+    po = np.zeros((dcp, dv))
+    pl = np.full(dcp, NEG_INF)
+    for r in range(dcp):
+        idx = shard_tokens(L, r, dcp, bs, I)
+        po[r], pl[r] = attention(q, K_all[idx], V_all[idx], scale)
+    o, lse = lse_merge(po, pl, sink)
+    return o, lse, po, pl
+
+
+def sparse_attention(q, K_all, V_all, scale, sel):
+    """Attention restricted to the selected global token ids (SFA, unsharded)."""
+    sel = np.asarray([g for g in sel if g >= 0 and g < K_all.shape[0]], dtype=np.int64)
+    return attention(q, K_all[sel], V_all[sel], scale)
+
+
+def sfa_sharded(q, K_all, V_all, scale, sel, L, dcp, bs, I, sink=None):
+    """SFA under DCP: each rank attends its owned selected tokens; merge with sink once."""
+    dv = V_all.shape[1]
+    po = np.zeros((dcp, dv))
+    pl = np.full(dcp, NEG_INF)
+    sel = np.asarray([g for g in sel if 0 <= g < L], dtype=np.int64)
+    owners = target_rank(sel, bs, dcp, I)
+    for r in range(dcp):
+        mine = sel[owners == r]
+        po[r], pl[r] = attention(q, K_all[mine], V_all[mine], scale)
+    o, lse = lse_merge(po, pl, sink)
+    return o, lse, po, pl
