@@ -1,0 +1,434 @@
+#!/usr/bin/env python3
+"""Benchmark of the DCP decode hot path on one GB300 (or N replicas).
+
+One step = one decode token per request through the whole path:
+per-rank context lengths, slot mapping of the B new tokens, owner-masked
+cache write, per-rank split-KV partial attention and the exact LSE merge
+(``dcp_local_seq_lens`` + ``dcp_slot_mapping`` + ``dcp_cache_write_*`` +
+``dcp_decode_*``), on the GQA workload B=32, Hq=32, Hkv=8, d=128, bf16,
+bimodal 1k-256k contexts, dcp=8, block_size 16 (other workloads with
+--config).  The KV cache is resident state, built once before timing.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config NAME] [--no-cpu-baseline]
+
+Prints one JSON line (rank 0).  ``value`` is KV-read GB/s of the step
+(KV bytes the step must read / device time), ``e2e`` the same metric with
+the per-step inputs copied from pinned host memory and the output copied
+back inside the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV-read GB/s & decode tok/s of sharded attn + LSE merge, % of roofline (1 GB300)"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def step_bytes(cfg, lens, B):
+    """(KV bytes, total algorithmic bytes) of one decode step."""
+    import numpy as np
+    es = 2 if cfg.dtype == "bf16" else 4
+    tokens = int(np.asarray(lens, dtype=np.int64).sum())
+    if cfg.kind == "gqa":
+        kv = tokens * cfg.Hkv * cfg.dk * 2 * es
+        new_tok = B * cfg.Hkv * cfg.dk * 2 * es * 2          # read + write of the new k/v rows
+    else:
+        kv = tokens * cfg.dk * es
+        new_tok = B * cfg.dk * es * 2
+    q = B * cfg.Hq * cfg.dk * es
+    out = B * cfg.Hq * cfg.dv * es + B * cfg.Hq * 4
+    partial = 2 * cfg.dcp * B * cfg.Hq * (cfg.dv + 1) * 4    # per-rank partials written + read
+    nvb = (np.asarray(lens, dtype=np.int64) + cfg.bs * cfg.dcp - 1) // (cfg.bs * cfg.dcp)
+    bt = int(nvb.sum()) * cfg.dcp * 4
+    return kv, kv + new_tok + q + out + partial + bt
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import context_paged_decode_gb300 as dcp
+    import workloads as W
+    from workloads import device as D
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = W.CONFIGS[args.config]
+    t0 = time.time()
+    wl = D.build(cfg, device=dev)
+    torch.cuda.synchronize()
+    setup_s = time.time() - t0
+    B = cfg.B
+    lay = wl.layout
+    tdt = D.torch_dtype(cfg.dtype)
+    stream = torch.cuda.current_stream()
+
+    # per-step inputs: the new token of every request sits at position L_b - 1
+    req = torch.arange(B, dtype=torch.int32, device=dev)
+    pos = (wl.seq_lens.to(torch.int64) - 1).contiguous()
+    if cfg.kind == "gqa":
+        newk = torch.empty((B, cfg.Hkv, cfg.dk), dtype=tdt, device=dev)
+        newv = torch.empty_like(newk)
+        row = cfg.Hkv * cfg.dk
+        for b in range(B):
+            x = int(wl.seq_lens_host[b]) - 1
+            D.fill(newk[b], cfg.seed, W.T_K, b, x * row, cfg.dtype)
+            D.fill(newv[b], cfg.seed, W.T_V, b, x * row, cfg.dtype)
+    else:
+        newk = torch.empty((B, cfg.dk), dtype=tdt, device=dev)
+        newv = None
+        for b in range(B):
+            x = int(wl.seq_lens_host[b]) - 1
+            D.fill(newk[b], cfg.seed, W.T_LATENT, b, x * cfg.dk, cfg.dtype)
+    kind = {"gqa": dcp.KIND_GQA, "mla": dcp.KIND_MLA, "sfa": dcp.KIND_SFA}[cfg.kind]
+    ws = torch.empty(dcp.decode_workspace_size(lay, kind, B, cfg.Hq, cfg.Hkv, cfg.dv),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((B, cfg.Hq, cfg.dv), dtype=tdt, device=dev)
+    out_lse = torch.empty((B, cfg.Hq), dtype=torch.float32, device=dev)
+    local = torch.empty((B, cfg.dcp), dtype=torch.int32, device=dev)
+    o_rank = torch.empty(B, dtype=torch.int32, device=dev)
+    o_slot = torch.empty((cfg.dcp, B), dtype=torch.int64, device=dev)
+    kv = wl.kv
+
+    def decode():
+        if cfg.kind == "gqa":
+            dcp.decode_gqa(lay, wl.q, kv, local, cfg.scale, sink=wl.sink, out=out,
+                           out_lse=out_lse, workspace=ws)
+        elif cfg.kind == "mla":
+            dcp.decode_mla(lay, wl.q, kv, local, cfg.scale, cfg.dv, sink=wl.sink, out=out,
+                           out_lse=out_lse, workspace=ws)
+        else:
+            dcp.sfa_decode(lay, wl.q, kv, wl.topk, wl.seq_lens, cfg.scale, cfg.dv, sink=wl.sink,
+                           out=out, out_lse=out_lse, workspace=ws)
+
+    def step():
+        dcp.local_seq_lens(lay, wl.seq_lens, out=local)
+        dcp.slot_mapping(lay, req, pos, wl.block_table, wl.num_blocks, out_rank=o_rank,
+                         out_slot=o_slot)
+        if cfg.kind == "gqa":
+            dcp.cache_write_gqa(lay, newk, newv, o_slot, wl.k_pools, wl.v_pools, wl.num_blocks)
+        else:
+            dcp.cache_write_mla(lay, newk, o_slot, wl.k_pools, wl.num_blocks)
+        decode()
+
+    launches_per_step = 3 + (3 if cfg.kind != "sfa" else 2)
+    kv_bytes, alg_bytes = step_bytes(cfg, wl.seq_lens_host, B)
+    if cfg.kind == "sfa":
+        kv_bytes = B * cfg.topk * cfg.dk * 2
+        alg_bytes = kv_bytes + B * cfg.Hq * cfg.dk * 2 + 2 * cfg.dcp * B * cfg.Hq * (cfg.dv + 1) * 4 \
+            + B * cfg.topk * 4 + B * cfg.Hq * (cfg.dv * 2 + 4)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # warm-up
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # timed steps (device time, CUDA events on the launching stream)
+    clk = Clocks(local_rank)
+    clk.start()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    step_ms = e0.elapsed_time(e1) / args.steps
+
+    # the dominant call alone: per-launch durations of the decode call
+    dec_ms = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        decode()
+        b.record(stream)
+        b.synchronize()
+        dec_ms.append(a.elapsed_time(b))
+    clocks = clk.stop()
+
+    # end to end: host inputs (pinned) -> device, step, output -> host
+    h_q = torch.empty(wl.q.shape, dtype=tdt, pin_memory=True)
+    h_q.copy_(wl.q)
+    h_k = torch.empty(newk.shape, dtype=tdt, pin_memory=True)
+    h_k.copy_(newk)
+    h_v = None
+    if newv is not None:
+        h_v = torch.empty(newv.shape, dtype=tdt, pin_memory=True)
+        h_v.copy_(newv)
+    h_pos = torch.empty(pos.shape, dtype=torch.int64, pin_memory=True)
+    h_pos.copy_(pos)
+    h_len = torch.empty(wl.seq_lens.shape, dtype=torch.int32, pin_memory=True)
+    h_len.copy_(wl.seq_lens)
+    h_out = torch.empty(out.shape, dtype=tdt, pin_memory=True)
+    h_lse = torch.empty(out_lse.shape, dtype=torch.float32, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_pos, h_len) if t is not None)
+    h2d += 0 if h_v is None else h_v.numel() * h_v.element_size()
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    def e2e_step():
+        wl.q.copy_(h_q, non_blocking=True)
+        newk.copy_(h_k, non_blocking=True)
+        if newv is not None:
+            newv.copy_(h_v, non_blocking=True)
+        pos.copy_(h_pos, non_blocking=True)
+        wl.seq_lens.copy_(h_len, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(out_lse, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = a.elapsed_time(b) / args.steps
+
+    if world > 1:
+        t = torch.tensor([step_ms, e2e_ms, statistics.mean(dec_ms)], dtype=torch.float64,
+                         device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms, e2e_ms, dec_avg = t.tolist()
+    else:
+        dec_avg = statistics.mean(dec_ms)
+
+    hbm_peak, peak_src = peaks()
+    achieved = alg_bytes / (dec_avg * 1e-3) / 1e9
+    value = world * kv_bytes / (step_ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded N(0,1) values; context lengths from the trace statistics)",
+        "config": {"workload": cfg.description, "name": cfg.name, "batch": B,
+                   "context_tokens": int(wl.seq_lens_host.astype("int64").sum()),
+                   "kv_bytes_per_step": kv_bytes, "l2": "inputs larger than L2 (KV >> 129 MB)"
+                   if kv_bytes > 512 << 20 else "working set fits L2; not flushed",
+                   "parallelism": f"dcp{cfg.dcp} virtual ranks on 1 GPU" +
+                                  (f" x {world} replicas" if world > 1 else "")},
+        "decode_tok_per_s": round(world * B / (step_ms * 1e-3), 1),
+        "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "roofline": {"bound": "hbm", "kernel": f"dcp_decode_{cfg.kind} (plan + split + merge)",
+                     "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "alg_bytes_per_launch": alg_bytes, "launch_ms": round(dec_avg, 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "setup_s": round(setup_s, 2),
+    }
+    return res, cfg, wl
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm, and the cpu_baseline of our arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(cfg, lens, budget_s, seed=0):
+    """Time the fp64 oracle on whole (request, head) problems until budget_s of
+    oracle compute; returns (KV bytes covered, seconds, description)."""
+    import numpy as np
+
+    import oracle as O
+    from tests import ref
+
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(len(lens))
+    done_bytes, spent, n = 0.0, 0.0, 0
+    G = cfg.Hq // cfg.Hkv if cfg.kind == "gqa" else cfg.Hq
+    es = 2 if cfg.dtype == "bf16" else 4
+    for b in order:
+        L = int(lens[b])
+        if cfg.kind == "gqa":
+            g = int(rng.integers(cfg.Hkv))
+            K, V = ref.gqa_kv(cfg, b, g, L)
+            heads = [g * G + i for i in range(G)]
+            unit_bytes = L * cfg.dk * 2 * es          # one kv head's K and V, read once per group
+        else:
+            K, V = ref.latent_kv(cfg, b, L)
+            heads = list(range(cfg.Hq))
+            unit_bytes = L * cfg.dk * es
+        qs = [ref.q_vec(cfg, b, h) for h in heads]
+        t0 = time.perf_counter()
+        for i, q in enumerate(qs):
+            O.sharded_attention(q, K, V, cfg.scale, L, cfg.dcp, cfg.bs, cfg.I)
+            if cfg.kind != "gqa" and time.perf_counter() - t0 + spent > budget_s:
+                unit_bytes *= (i + 1) / len(qs)
+                break
+        spent += time.perf_counter() - t0
+        done_bytes += unit_bytes
+        n += 1
+        if spent > budget_s:
+            break
+    what = (f"{n} requests x one kv head group ({G} q heads), full context, fp64 oracle"
+            if cfg.kind == "gqa" else f"{n} requests x all {cfg.Hq} heads (last partial), fp64")
+    return done_bytes, spent, what
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle (no reference implementation exists)."""
+    import workloads as W
+
+    cfg = W.CONFIGS[args.config]
+    lens = W.make_seq_lens(cfg)
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup):
+        oracle_sample(cfg, lens, per_step, seed=100 + i)
+    tot_b, tot_s, what = 0.0, 0.0, ""
+    for i in range(args.steps):
+        b, s, what = oracle_sample(cfg, lens, per_step, seed=i)
+        tot_b += b
+        tot_s += s
+    v = tot_b / tot_s / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_s / max(1, args.steps), 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.description, "name": cfg.name},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": f"per step: {what}"},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="gqa_bf16_b32")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res, cfg, wl = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            b, s, what = oracle_sample(cfg, wl.seq_lens_host, args.cpu_budget)
+            res["cpu_baseline"] = {"value": round(b / s / 1e9, 4), "unit": "GB/s",
+                                   "cores": os.cpu_count(), "kind": "oracle",
+                                   "sample": what + f", {s:.1f} s"}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,145 @@
+// Exact LSE merge of partial attention results (+ optional sink applied once).
+//
+// Page "Decode Context Parallel (DCP)", section "Backend structure" (the
+// common partial-output/LSE merge) and page "DeepSeek V4.1 context
+// parallelism", section "Decode computation" (the sink is applied once when
+// the partial outputs are merged by log-sum-exp):
+//     lse = ln(sum_i exp(lse_i) + exp(sink)),  o = sum_i exp(lse_i - lse) o_i.
+// HBM-bound: one warp per output row, 16-byte loads of the partials.
+#include "dcp_common.cuh"
+
+namespace dcp {
+
+struct DenseParts {  // part_o [n][B][H][dv], part_lse [n][B][H]
+  const float* o;
+  const float* lse;
+  int64_t stride;  // B*H
+  __device__ __forceinline__ float lse_at(int i, int64_t row) const { return lse[i * stride + row]; }
+  __device__ __forceinline__ const float* o_at(int i, int64_t row, int dv) const {
+    return o + (i * stride + row) * dv;
+  }
+};
+
+struct ItemParts {  // plan items: lse [item][G], o [item][G][dv]
+  const float* o;
+  const float* lse;
+  int first, G, hh;
+  __device__ __forceinline__ float lse_at(int i, int64_t) const {
+    return lse[(int64_t)(first + i) * G + hh];
+  }
+  __device__ __forceinline__ const float* o_at(int i, int64_t, int dv) const {
+    return o + ((int64_t)(first + i) * G + hh) * dv;
+  }
+};
+
+template <class Parts>
+__device__ __forceinline__ void merge_row(const Parts& P, int n, int64_t row, int dv,
+                                          bool has_sink, float sink, void* out, int out_dtype,
+                                          int64_t out_row, float* out_lse) {
+  const int lane = threadIdx.x & 31;
+  float m = has_sink ? sink : -INFINITY;
+  for (int i = lane; i < n; i += 32) m = fmaxf(m, P.lse_at(i, row));
+  m = warp_max(m);
+  const int nv = dv >> 2;
+  if (m == -INFINITY) {  // nothing attended and no sink
+    for (int c = lane; c < nv; c += 32) {
+      if (out_dtype == DCP_F32)
+        reinterpret_cast<float4*>(out)[out_row * nv + c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      else
+        reinterpret_cast<uint2*>(out)[out_row * nv + c] = make_uint2(0u, 0u);
+    }
+    if (out_lse && lane == 0) out_lse[out_row] = -INFINITY;
+    return;
+  }
+  float s = 0.f;
+  for (int i = lane; i < n; i += 32) {
+    const float l = P.lse_at(i, row);
+    if (l != -INFINITY) s += expf(l - m);
+  }
+  s = warp_sum(s);  // identical on every lane
+  if (has_sink) s += expf(sink - m);
+  const float lse = m + logf(s);
+  for (int c = lane; c < nv; c += 32) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < n; ++i) {
+      const float l = P.lse_at(i, row);
+      if (l == -INFINITY) continue;
+      const float w = expf(l - lse);
+      const float4 v = __ldg(reinterpret_cast<const float4*>(P.o_at(i, row, dv)) + c);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    if (out_dtype == DCP_F32)
+      reinterpret_cast<float4*>(out)[out_row * nv + c] = acc;
+    else
+      reinterpret_cast<uint2*>(out)[out_row * nv + c] =
+          make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+  }
+  if (out_lse && lane == 0) out_lse[out_row] = lse;
+}
+
+__global__ void dense_merge_kernel(int n, const float* __restrict__ po,
+                                   const float* __restrict__ pl, int B, int H, int dv,
+                                   const float* __restrict__ sink, void* out, int out_dtype,
+                                   float* out_lse) {
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= (int64_t)B * H) return;
+  const int h = (int)(row % H);
+  DenseParts P{po, pl, (int64_t)B * H};
+  merge_row(P, n, row, dv, sink != nullptr, sink ? sink[h] : 0.f, out, out_dtype, row, out_lse);
+}
+
+// mode 0: row = (b, h), parts = all items of (b, g) over every rank; sink applies.
+// mode 1: row = (r, b, h), parts = items of (b, g, r); output is float32 per rank.
+__global__ void item_merge_kernel(Plan plan, int mode, int B, int dcp, int Hq, int G, int groups,
+                                  int dv, const float* __restrict__ sink, void* out,
+                                  int out_dtype, float* out_lse) {
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t nrows = (int64_t)(mode == 0 ? 1 : dcp) * B * Hq;
+  if (row >= nrows) return;
+  const int h = (int)(row % Hq);
+  const int b = (int)((row / Hq) % B);
+  const int r = mode == 0 ? 0 : (int)(row / ((int64_t)B * Hq));
+  const int g = h / G, hh = h % G;
+  const int e = (b * groups + g) * dcp;
+  const int first = plan.off[e + r];
+  const int last = plan.off[e + (mode == 0 ? dcp : r + 1)];
+  ItemParts P{plan.o, plan.lse, first, G, hh};
+  const bool hs = (mode == 0) && sink != nullptr;
+  merge_row(P, last - first, row, dv, hs, hs ? sink[h] : 0.f, out,
+            mode == 0 ? out_dtype : (int)DCP_F32, row, out_lse);
+}
+
+int launch_item_merge(const Plan& plan, int mode, int B, int dcp, int Hq, int G, int groups,
+                      int dv, const float* sink, void* out, int out_dtype, float* out_lse,
+                      cudaStream_t s) {
+  const int64_t rows = (int64_t)(mode == 0 ? 1 : dcp) * B * Hq;
+  if (rows == 0) return DCP_OK;
+  const int wpb = 8;
+  item_merge_kernel<<<(unsigned)((rows + wpb - 1) / wpb), wpb * 32, 0, s>>>(
+      plan, mode, B, dcp, Hq, G, groups, dv, sink, out, out_dtype, out_lse);
+  return launch_status();
+}
+
+}  // namespace dcp
+
+using namespace dcp;
+
+extern "C" int dcp_lse_merge(int32_t num_parts, const float* part_o, const float* part_lse,
+                             int32_t num_reqs, int32_t num_heads, int32_t head_dim_v,
+                             const float* sink, void* out, dcp_dtype_t out_dtype, float* out_lse,
+                             dcp_stream_t stream) {
+  if (num_parts < 0 || num_reqs < 0 || num_heads < 0 || head_dim_v < 4 || head_dim_v % 4 != 0 ||
+      head_dim_v > 1024 || (out_dtype != DCP_F32 && out_dtype != DCP_BF16))
+    return DCP_EINVAL;
+  const int64_t rows = (int64_t)num_reqs * num_heads;
+  if (rows == 0) return DCP_OK;
+  if (!out || (num_parts > 0 && (!part_o || !part_lse))) return DCP_EINVAL;
+  const int wpb = 8;
+  dense_merge_kernel<<<(unsigned)((rows + wpb - 1) / wpb), wpb * 32, 0, (cudaStream_t)stream>>>(
+      num_parts, part_o, part_lse, num_reqs, num_heads, head_dim_v, sink, out, (int)out_dtype,
+      out_lse);
+  return launch_status();
+}

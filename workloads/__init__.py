@@ -67,7 +67,7 @@ def _mix64_np(z: np.ndarray) -> np.ndarray:
 
 
 def stream_key(seed: int, tensor: int, request: int) -> int:
-    return mix64_int(seed * _G1 + tensor * _G2 + request * _G3 + _G4)
+    return mix64_int(int(seed) * _G1 + int(tensor) * _G2 + int(request) * _G3 + _G4)
 
 
 _TABLES: dict = {}
