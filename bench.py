@@ -137,6 +137,10 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     cfg = W.CONFIGS[args.config]
+    if args.reqs:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, B=args.reqs,
+                                  lengths=[int(x) for x in W.make_seq_lens(cfg)[:args.reqs]])
     t0 = time.time()
     wl = D.build(cfg, device=dev)
     torch.cuda.synchronize()
@@ -400,12 +404,14 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="gqa_bf16_b32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--reqs", type=int, default=0,
+                    help="keep only the first N requests of the workload (profiling cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local_rank = dist_env()

@@ -98,3 +98,67 @@ def test_sfa_full_size_sampled(lib):
         exp = ref.sfa_expected(SFA, wl.seq_lens_host, wl.topk_host, int(b), heads, sink=sink)
         for h in heads:
             ref.check_bf16(out[b, h], lse[b, h], exp[h][0], exp[h][1], f"b{b} h{h}")
+
+
+def mla_sampled(lib, cfg, reqs, heads_per_req, seed):
+    wl = D.build(cfg)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = lib.decode_mla(wl.layout, wl.q, wl.kv, wl.local_lens, cfg.scale, cfg.dv, err=err)
+    po, pl = lib.decode_partial_mla(wl.layout, wl.q, wl.kv, wl.local_lens, cfg.scale, cfg.dv,
+                                    err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    po, pl = po.cpu().numpy(), pl.cpu().numpy()
+    rng = np.random.default_rng(seed)
+    for b in reqs:
+        heads = sorted(rng.choice(cfg.Hq, heads_per_req, replace=False).tolist())
+        exp = ref.mla_expected(cfg, wl.seq_lens_host, b, heads)
+        for h in heads:
+            o_ref, lse_ref, po_ref, pl_ref = exp[h]
+            ref.check_bf16(out[b, h], lse[b, h], o_ref, lse_ref, f"b{b} h{h}")
+            for r in range(cfg.dcp):
+                ref.check_bf16(po[r, b, h], pl[r, b, h], po_ref[r], pl_ref[r], f"r{r} b{b} h{h}")
+
+
+def test_mla_bf16_b64_full_size_sampled(lib):
+    lens = W.make_seq_lens(MLA)
+    order = np.argsort(lens)
+    reqs = sorted({int(order[0]), int(order[-1]), int(order[len(order) // 2]), 7})
+    mla_sampled(lib, MLA, reqs, 3, seed=0)
+
+
+def test_longtail_mla_sampled(lib):
+    mla_sampled(lib, W.CONFIGS["longtail_mla"], [0, 1, 2, 3], 2, seed=1)
+
+
+@pytest.mark.parametrize("dcp_size", [1, 2])
+def test_mla_online_softmax_rescale(lib, dcp_size):
+    """Scores that keep growing along the sequence (and one dominant late
+    token) force the output to be rescaled many times."""
+    import context_paged_decode_gb300 as dcp
+    import oracle as O
+    cfg = dataclasses.replace(MLA, B=1, lengths=[3000], dcp=dcp_size, bs=64, I=1)
+    rng = np.random.default_rng(11)
+    L = 3000
+    q = rng.standard_normal((1, 128, 576)).astype(np.float32)
+    kv = rng.standard_normal((L, 576)).astype(np.float32)
+    kv[:, :] *= (1.0 + 6.0 * np.arange(L) / L)[:, None]
+    kv[2500] = q[0, 5] * 0.2                              # one token that dominates head 5
+    qb = W.f32_to_bf16_bits(q)
+    kvb = W.f32_to_bf16_bits(kv)
+    wl = D.build(cfg, populate=False)
+    wl.q.view(torch.int16).copy_(torch.from_numpy(qb.view(np.int16)))
+    req = torch.zeros(L, dtype=torch.int32, device="cuda")
+    pos = torch.arange(L, dtype=torch.int64, device="cuda")
+    _, slot = dcp.slot_mapping(wl.layout, req, pos, wl.block_table, wl.num_blocks)
+    kvd = torch.from_numpy(kvb.view(np.int16)).cuda().view(torch.bfloat16)
+    dcp.cache_write_mla(wl.layout, kvd, slot, wl.k_pools, wl.num_blocks)
+    out, lse = lib.decode_mla(wl.layout, wl.q, wl.kv, wl.local_lens, cfg.scale, 512,
+                              out_dtype=torch.float32)
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    K = W.as_float64(kvb, "bf16")
+    for h in [0, 5, 77, 127]:
+        qv = W.as_float64(qb[0, h], "bf16")
+        o_ref, lse_ref = O.attention(qv, K, K[:, :512], cfg.scale)
+        ref.check_bf16(out[0, h], lse[0, h], o_ref, lse_ref, f"h{h}")
