@@ -76,6 +76,8 @@ def load(path: str = LIB_PATH):
         "dcp_lse_merge": (C.c_int, [i32, vp, vp, i32, i32, i32, vp, vp, C.c_int, vp, vp]),
         "dcp_decode_gqa": (C.c_int, [L, vp, i32, i32, i32, i32, f32, C.c_int, PK, vp, vp, vp,
                                      C.c_int, vp, vp, C.c_size_t, vp, vp]),
+        "dcp_decode_gqa_noalloc": (C.c_int, [L, vp, i32, i32, i32, i32, f32, C.c_int, PK, vp, vp,
+                                             vp, C.c_int, vp, vp, vp]),
         "dcp_decode_partial_mla": (C.c_int, [L, vp, i32, i32, i32, i32, f32, C.c_int, PK, vp, vp,
                                              vp, vp, C.c_size_t, vp, vp]),
         "dcp_decode_mla": (C.c_int, [L, vp, i32, i32, i32, i32, f32, C.c_int, PK, vp, vp, vp,
@@ -98,7 +100,8 @@ def exported_symbols():
     """Names of the C entry points this binding expects the library to export."""
     return ["dcp_strerror", "dcp_version", "dcp_local_seq_lens", "dcp_slot_mapping",
             "dcp_cache_write_gqa", "dcp_cache_write_mla", "dcp_decode_workspace_size",
-            "dcp_decode_partial_gqa", "dcp_lse_merge", "dcp_decode_gqa", "dcp_decode_partial_mla",
+            "dcp_decode_partial_gqa", "dcp_lse_merge", "dcp_decode_gqa", "dcp_decode_gqa_noalloc",
+            "dcp_decode_partial_mla",
             "dcp_decode_mla", "dcp_sfa_remap", "dcp_sfa_decode_partial", "dcp_sfa_decode"]
 
 
@@ -272,6 +275,27 @@ def decode_gqa(layout, q, kv: PagedKV, local_lens, scale, sink=None, out_dtype=N
     _check(lib.dcp_decode_gqa(layout, _p(q), B, Hq, Hkv, d, float(scale), _dtype(q), kv.struct(),
                               _p(local_lens), _p(sink), _p(out), _dtype(out), _p(out_lse),
                               _p(ws), ws.numel(), _p(err), _stream(stream)))
+    return out, out_lse
+
+
+def decode_gqa_noalloc(layout, q, kv: PagedKV, local_lens, scale, sink=None, out_dtype=None,
+                       out=None, out_lse=None, err=None, stream=None):
+    """dcp_decode_gqa without a caller workspace: the library's fixed 16 MiB
+    device array holds the split-KV scratch (for callers that cannot allocate;
+    calls that overlap on the GPU race on that array)."""
+    lib = load()
+    _cuda_contig(q, local_lens, sink)
+    B, Hq, d = q.shape
+    Hkv = kv.k_pools[0].shape[1]
+    dev = q.device
+    odt = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=odt, device=dev)
+    if out_lse is None:
+        out_lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    _check(lib.dcp_decode_gqa_noalloc(layout, _p(q), B, Hq, Hkv, d, float(scale), _dtype(q),
+                                      kv.struct(), _p(local_lens), _p(sink), _p(out),
+                                      _dtype(out), _p(out_lse), _p(err), _stream(stream)))
     return out, out_lse
 
 

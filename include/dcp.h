@@ -248,6 +248,35 @@ int dcp_decode_gqa(dcp_layout_t layout, const void* q, int32_t num_reqs, int32_t
                    size_t workspace_bytes, int32_t* err_count, dcp_stream_t stream);
 
 /*
+ * dcp_decode_gqa_noalloc -- dcp_decode_gqa without a caller workspace.  The
+ * pages have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory when they decode (a runtime that owns all device
+ * memory and gives the library none, code running under a fixed memory
+ * budget, or a C caller with no device allocator).  The split-KV workspace
+ * comes from a fixed 16 MiB array inside the library's own device memory,
+ * which every GPU that loads the library holds until the process exits.
+ * Arguments and results are those of dcp_decode_gqa.
+ *  - Returns DCP_EWORKSPACE, launching nothing, when the batch needs more
+ *    than 16 MiB of workspace (dcp_decode_workspace_size tells in advance).
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before
+ *    any stream capture.
+ *  - Every call on a device uses the same array: calls that overlap on the
+ *    GPU (different streams, concurrent graphs) race and corrupt each
+ *    other's results.  Calls in one stream order are safe.  The array keeps
+ *    the last call's contents; each call rewrites every counter it reads
+ *    (in stream order, before its kernels use them), so nothing needs
+ *    clearing between calls.
+ *  - Allocates nothing: no cudaMalloc, no cudaFree.
+ */
+int dcp_decode_gqa_noalloc(dcp_layout_t layout, const void* q, int32_t num_reqs,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           float scale, dcp_dtype_t dtype, dcp_paged_kv_t kv,
+                           const int32_t* local_lens, const float* sink, void* out,
+                           dcp_dtype_t out_dtype, float* out_lse, int32_t* err_count,
+                           dcp_stream_t stream);
+
+/*
  * dcp_decode_partial_mla -- per-rank partial decode attention for MLA
  * (vLLM DCP blog post, section 1: one latent KV head shared by every query
  * head, which tensor parallelism cannot split, so DCP splits it by
