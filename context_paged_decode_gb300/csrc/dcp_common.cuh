@@ -5,7 +5,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "../../include/dcp.h"
+#include "dcp.h"
 
 namespace dcp {
 
