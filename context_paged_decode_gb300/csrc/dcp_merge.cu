@@ -32,7 +32,11 @@ struct ItemParts {  // plan items: lse [item][G], o [item][G][dv]
   }
 };
 
-template <class Parts>
+// One warp per output row.  Lane i computes the weight of part i (in blocks of
+// 32 parts) once; the weights are broadcast with shuffles while every lane
+// accumulates CH float4 columns, four parts per iteration so several loads
+// are in flight.
+template <int CH, class Parts>
 __device__ __forceinline__ void merge_row(const Parts& P, int n, int64_t row, int dv,
                                           bool has_sink, float sink, void* out, int out_dtype,
                                           int64_t out_row, float* out_lse) {
@@ -59,27 +63,50 @@ __device__ __forceinline__ void merge_row(const Parts& P, int n, int64_t row, in
   s = warp_sum(s);  // identical on every lane
   if (has_sink) s += expf(sink - m);
   const float lse = m + logf(s);
-  for (int c = lane; c < nv; c += 32) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < n; ++i) {
-      const float l = P.lse_at(i, row);
-      if (l == -INFINITY) continue;
-      const float w = expf(l - lse);
-      const float4 v = __ldg(reinterpret_cast<const float4*>(P.o_at(i, row, dv)) + c);
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+  float4 acc[CH];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int blk = 0; blk < n; blk += 32) {
+    float wl = 0.f;
+    if (blk + lane < n) {
+      const float l = P.lse_at(blk + lane, row);
+      wl = l == -INFINITY ? 0.f : expf(l - lse);
     }
-    if (out_dtype == DCP_F32)
-      reinterpret_cast<float4*>(out)[out_row * nv + c] = acc;
-    else
-      reinterpret_cast<uint2*>(out)[out_row * nv + c] =
-          make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+    const int cnt = min(32, n - blk);
+#pragma unroll 4
+    for (int ii = 0; ii < cnt; ++ii) {
+      const float w = __shfl_sync(0xffffffffu, wl, ii);
+      const float4* src = reinterpret_cast<const float4*>(P.o_at(blk + ii, row, dv));
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int idx = lane + 32 * c;
+        if (idx < nv) {
+          const float4 v = __ldg(src + idx);
+          if (w != 0.f) {  // an empty part adds nothing, whatever its o holds
+            acc[c].x = fmaf(w, v.x, acc[c].x);
+            acc[c].y = fmaf(w, v.y, acc[c].y);
+            acc[c].z = fmaf(w, v.z, acc[c].z);
+            acc[c].w = fmaf(w, v.w, acc[c].w);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int idx = lane + 32 * c;
+    if (idx < nv) {
+      if (out_dtype == DCP_F32)
+        reinterpret_cast<float4*>(out)[out_row * nv + idx] = acc[c];
+      else
+        reinterpret_cast<uint2*>(out)[out_row * nv + idx] =
+            make_uint2(pack_bf16(acc[c].x, acc[c].y), pack_bf16(acc[c].z, acc[c].w));
+    }
   }
   if (out_lse && lane == 0) out_lse[out_row] = lse;
 }
 
+template <int CH>
 __global__ void dense_merge_kernel(int n, const float* __restrict__ po,
                                    const float* __restrict__ pl, int B, int H, int dv,
                                    const float* __restrict__ sink, void* out, int out_dtype,
@@ -88,11 +115,13 @@ __global__ void dense_merge_kernel(int n, const float* __restrict__ po,
   if (row >= (int64_t)B * H) return;
   const int h = (int)(row % H);
   DenseParts P{po, pl, (int64_t)B * H};
-  merge_row(P, n, row, dv, sink != nullptr, sink ? sink[h] : 0.f, out, out_dtype, row, out_lse);
+  merge_row<CH>(P, n, row, dv, sink != nullptr, sink ? sink[h] : 0.f, out, out_dtype, row,
+                out_lse);
 }
 
 // mode 0: row = (b, h), parts = all items of (b, g) over every rank; sink applies.
 // mode 1: row = (r, b, h), parts = items of (b, g, r); output is float32 per rank.
+template <int CH>
 __global__ void item_merge_kernel(Plan plan, int mode, int B, int dcp, int Hq, int G, int groups,
                                   int dv, const float* __restrict__ sink, void* out,
                                   int out_dtype, float* out_lse) {
@@ -108,7 +137,7 @@ __global__ void item_merge_kernel(Plan plan, int mode, int B, int dcp, int Hq, i
   const int last = plan.off[e + (mode == 0 ? dcp : r + 1)];
   ItemParts P{plan.o, plan.lse, first, G, hh};
   const bool hs = (mode == 0) && sink != nullptr;
-  merge_row(P, last - first, row, dv, hs, hs ? sink[h] : 0.f, out,
+  merge_row<CH>(P, last - first, row, dv, hs, hs ? sink[h] : 0.f, out,
             mode == 0 ? out_dtype : (int)DCP_F32, row, out_lse);
 }
 
@@ -118,8 +147,20 @@ int launch_item_merge(const Plan& plan, int mode, int B, int dcp, int Hq, int G,
   const int64_t rows = (int64_t)(mode == 0 ? 1 : dcp) * B * Hq;
   if (rows == 0) return DCP_OK;
   const int wpb = 8;
-  item_merge_kernel<<<(unsigned)((rows + wpb - 1) / wpb), wpb * 32, 0, s>>>(
-      plan, mode, B, dcp, Hq, G, groups, dv, sink, out, out_dtype, out_lse);
+  const unsigned grid = (unsigned)((rows + wpb - 1) / wpb);
+  const int nv = dv / 4;
+  if (nv <= 32)
+    item_merge_kernel<1><<<grid, wpb * 32, 0, s>>>(plan, mode, B, dcp, Hq, G, groups, dv, sink,
+                                                   out, out_dtype, out_lse);
+  else if (nv <= 64)
+    item_merge_kernel<2><<<grid, wpb * 32, 0, s>>>(plan, mode, B, dcp, Hq, G, groups, dv, sink,
+                                                   out, out_dtype, out_lse);
+  else if (nv <= 128)
+    item_merge_kernel<4><<<grid, wpb * 32, 0, s>>>(plan, mode, B, dcp, Hq, G, groups, dv, sink,
+                                                   out, out_dtype, out_lse);
+  else
+    item_merge_kernel<8><<<grid, wpb * 32, 0, s>>>(plan, mode, B, dcp, Hq, G, groups, dv, sink,
+                                                   out, out_dtype, out_lse);
   return launch_status();
 }
 
@@ -138,8 +179,24 @@ extern "C" int dcp_lse_merge(int32_t num_parts, const float* part_o, const float
   if (rows == 0) return DCP_OK;
   if (!out || (num_parts > 0 && (!part_o || !part_lse))) return DCP_EINVAL;
   const int wpb = 8;
-  dense_merge_kernel<<<(unsigned)((rows + wpb - 1) / wpb), wpb * 32, 0, (cudaStream_t)stream>>>(
-      num_parts, part_o, part_lse, num_reqs, num_heads, head_dim_v, sink, out, (int)out_dtype,
-      out_lse);
+  const unsigned grid = (unsigned)((rows + wpb - 1) / wpb);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int nv = head_dim_v / 4;
+  if (nv <= 32)
+    dense_merge_kernel<1><<<grid, wpb * 32, 0, st>>>(num_parts, part_o, part_lse, num_reqs,
+                                                     num_heads, head_dim_v, sink, out,
+                                                     (int)out_dtype, out_lse);
+  else if (nv <= 64)
+    dense_merge_kernel<2><<<grid, wpb * 32, 0, st>>>(num_parts, part_o, part_lse, num_reqs,
+                                                     num_heads, head_dim_v, sink, out,
+                                                     (int)out_dtype, out_lse);
+  else if (nv <= 128)
+    dense_merge_kernel<4><<<grid, wpb * 32, 0, st>>>(num_parts, part_o, part_lse, num_reqs,
+                                                     num_heads, head_dim_v, sink, out,
+                                                     (int)out_dtype, out_lse);
+  else
+    dense_merge_kernel<8><<<grid, wpb * 32, 0, st>>>(num_parts, part_o, part_lse, num_reqs,
+                                                     num_heads, head_dim_v, sink, out,
+                                                     (int)out_dtype, out_lse);
   return launch_status();
 }

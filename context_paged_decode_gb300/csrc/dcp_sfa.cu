@@ -7,7 +7,10 @@
 // and decode-only batches keep the Q-gather and result-merge path.  The
 // attention sink is applied once, at the merge (page "DeepSeek V4.1 context
 // parallelism", section "Decode computation").
+#include <string.h>
+
 #include "dcp_generic.cuh"
+#include "dcp_sfa_mma.cuh"
 
 using namespace dcp;
 
@@ -48,6 +51,40 @@ GenericArgs sfa_generic_args(const dcp_layout_t& layout, const void* q, int B, i
   return A;
 }
 
+bool sfa_fast_ok(const dcp_layout_t& layout, const void* q, int Hq, int dk, int dv,
+                 dcp_dtype_t dtype, const dcp_paged_kv_t& kv, int K) {
+  if (!sfa_mma_supported(Hq, dk, dv, dtype, K)) return false;
+  if ((int64_t)kv.num_blocks * layout.block_size >= (int64_t(1) << 31)) return false;
+  if ((uintptr_t)q & 15) return false;
+  for (int r = 0; r < layout.dcp_size; ++r)
+    if ((uintptr_t)kv.k.ptr[r] & 15) return false;
+  return true;
+}
+
+SfaMmaArgs sfa_mma_args(const dcp_layout_t& layout, const void* q, int B, int Hq, float scale,
+                        const dcp_paged_kv_t& kv, int K, float* part_o, float* part_lse,
+                        int32_t* err) {
+  SfaMmaArgs A;
+  memset(&A, 0, sizeof(A));
+  A.q = (const __nv_bfloat16*)q;
+  A.B = B;
+  A.Hq = Hq;
+  A.dcp = layout.dcp_size;
+  A.bs = layout.block_size;
+  A.K = K;
+  A.sl2 = scale * kLog2e;
+  A.pool = kv.k;
+  A.num_blocks = kv.num_blocks;
+  A.bt = kv.block_table;
+  A.max_vb = kv.max_vblocks;
+  A.bt_rank_stride = kv.bt_rank_stride;
+  A.L = Layout{layout.dcp_size, layout.block_size, layout.interleave};
+  A.part_o = part_o;
+  A.part_lse = part_lse;
+  A.err = err;
+  return A;
+}
+
 }  // namespace
 
 extern "C" {
@@ -61,6 +98,13 @@ int dcp_sfa_decode_partial(dcp_layout_t layout, const void* q, int32_t num_reqs,
     return DCP_EINVAL;
   if (num_reqs == 0) return DCP_OK;
   if (!part_o || !part_lse || (topk_len > 0 && (!sel_rank || !sel_slot))) return DCP_EINVAL;
+  if (sfa_fast_ok(layout, q, num_q_heads, kv_dim, v_dim, dtype, kv, topk_len)) {
+    SfaMmaArgs M = sfa_mma_args(layout, q, num_reqs, num_q_heads, scale, kv, topk_len, part_o,
+                                part_lse, err_count);
+    M.sel_rank = sel_rank;
+    M.sel_slot = sel_slot;
+    return launch_sfa_mma(M, (cudaStream_t)stream);
+  }
   const GenericArgs A =
       sfa_generic_args(layout, q, num_reqs, num_q_heads, kv_dim, v_dim, scale, kv, err_count);
   SfaSel S{sel_rank, sel_slot, nullptr, nullptr, topk_len,
@@ -89,11 +133,20 @@ int dcp_sfa_decode(dcp_layout_t layout, const void* q, int32_t num_reqs, int32_t
       (float*)((char*)workspace +
                align_up(sizeof(float) * (size_t)dcp * num_reqs * num_q_heads * v_dim, 256));
   cudaStream_t s = (cudaStream_t)stream;
-  const GenericArgs A =
-      sfa_generic_args(layout, q, num_reqs, num_q_heads, kv_dim, v_dim, scale, kv, err_count);
-  SfaSel S{nullptr, nullptr, topk, seq_lens, topk_len,
-           Layout{layout.dcp_size, layout.block_size, layout.interleave}};
-  int rc = launch_sfa_generic(A, S, part_o, part_lse, dtype == DCP_BF16, s);
+  int rc;
+  if (sfa_fast_ok(layout, q, num_q_heads, kv_dim, v_dim, dtype, kv, topk_len)) {
+    SfaMmaArgs M = sfa_mma_args(layout, q, num_reqs, num_q_heads, scale, kv, topk_len, part_o,
+                                part_lse, err_count);
+    M.topk = topk;
+    M.seq_lens = seq_lens;
+    rc = launch_sfa_mma(M, s);
+  } else {
+    const GenericArgs A =
+        sfa_generic_args(layout, q, num_reqs, num_q_heads, kv_dim, v_dim, scale, kv, err_count);
+    SfaSel S{nullptr, nullptr, topk, seq_lens, topk_len,
+             Layout{layout.dcp_size, layout.block_size, layout.interleave}};
+    rc = launch_sfa_generic(A, S, part_o, part_lse, dtype == DCP_BF16, s);
+  }
   if (rc) return rc;
   return dcp_lse_merge(dcp, part_o, part_lse, num_reqs, num_q_heads, v_dim, sink, out, out_dtype,
                        out_lse, stream);

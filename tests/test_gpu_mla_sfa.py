@@ -56,6 +56,8 @@ SFA_SMALL = [
     dataclasses.replace(SFA, B=3, lengths=[5000, 900, 2048], topk=256, dcp=4, bs=64, I=1),
     dataclasses.replace(SFA, B=2, Hq=8, dtype="f32", lengths=[400, 64], topk=32, dcp=2, bs=16,
                         I=16),
+    dataclasses.replace(SFA, B=2, Hq=128, lengths=[9000, 300], topk=200, dcp=4, bs=64, I=64),
+    dataclasses.replace(SFA, B=3, Hq=16, lengths=[3000, 17, 640], topk=16, dcp=2, bs=16, I=4),
 ]
 
 
