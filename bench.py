@@ -40,13 +40,50 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", 0))
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# DRAM traffic of the dominant kernel from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), taken on a smaller case of the same workload and
+# scaled to a full launch by the KV bytes processed (traffic grows in
+# proportion: the kernel reads each KV byte once).  Valid only while the
+# kernel source is the one captured (sha256 prefix); otherwise null.
+NCU_TRAFFIC = {
+    "gqa_bf16_b32": {"source": "context_paged_decode_gb300/csrc/dcp_gqa.cu",
+                     "sha256_16": "d84b9510e12045c1", "dram_bytes": 1159449344 + 6443264,
+                     "kv_bytes": 282732 * 4096,
+                     "capture": "profiles/gqa_tma_kernel_gqa_bf16_b32.md"},
+}
+
+
+def traffic_per_launch(name, kv_bytes):
+    import hashlib
+    e = NCU_TRAFFIC.get(name)
+    if not e:
+        return None
+    with open(os.path.join(ROOT, e["source"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != e["sha256_16"]:
+            return None
+    return int(e["dram_bytes"] * kv_bytes / e["kv_bytes"])
+
+
 def peaks():
+    """(HBM GB/s, bf16 dense TFLOP/s burst, source)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def step_flops(cfg, lens, B):
+    """Algorithmic tensor flops of one decode step (Q.K^T + P.V, all heads)."""
+    import numpy as np
+    if cfg.kind == "sfa":
+        tokens = B * cfg.topk
+    else:
+        tokens = int(np.asarray(lens, dtype=np.int64).sum())
+    return tokens * cfg.Hq * (2 * cfg.dk + 2 * cfg.dv)
 
 
 class Clocks:
@@ -64,7 +101,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -95,6 +132,27 @@ class Clocks:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# whole-job aggregation over ranks (replicas)
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank timings over the default process group
+    (identity without one).  Every rank gets the result."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_value(units_per_rank, world, seconds):
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return world * units_per_rank / seconds
 
 
 # ---------------------------------------------------------------------------
@@ -282,17 +340,16 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     e2e_ms = a.elapsed_time(b) / args.steps
 
-    if world > 1:
-        t = torch.tensor([step_ms, e2e_ms, statistics.mean(dec_ms)], dtype=torch.float64,
-                         device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms, e2e_ms, dec_avg = t.tolist()
-    else:
-        dec_avg = statistics.mean(dec_ms)
+    step_ms, e2e_ms, dec_avg = max_over_ranks([step_ms, e2e_ms, statistics.mean(dec_ms)],
+                                              device=dev if world > 1 else None)
 
-    hbm_peak, peak_src = peaks()
+    hbm_peak, tc_peak, peak_src = peaks()
+    flops = step_flops(cfg, wl.seq_lens_host, B)
+    t_hbm = alg_bytes / (hbm_peak * 1e9)
+    t_tc = flops / (tc_peak * 1e12)
+    tensor_bound = cfg.kind != "gqa" and t_tc > t_hbm
     achieved = alg_bytes / (dec_avg * 1e-3) / 1e9
-    value = world * kv_bytes / (step_ms * 1e-3) / 1e9
+    value = job_value(kv_bytes, world, step_ms * 1e-3) / 1e9
     res = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -312,16 +369,25 @@ def run_ours(args, rank, world, local_rank):
                    if kv_bytes > 512 << 20 else "working set fits L2; not flushed",
                    "parallelism": f"dcp{cfg.dcp} virtual ranks on 1 GPU" +
                                   (f" x {world} replicas" if world > 1 else "")},
-        "decode_tok_per_s": round(world * B / (step_ms * 1e-3), 1),
-        "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "decode_tok_per_s": round(job_value(B, world, step_ms * 1e-3), 1),
+        "e2e": {"value": round(job_value(kv_bytes, world, e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "roofline": {"bound": "hbm", "kernel": f"dcp_decode_{cfg.kind} (plan + split + merge)",
-                     "achieved": round(achieved, 1), "peak": hbm_peak,
-                     "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4), "traffic": None,
-                     "alg_bytes_per_launch": alg_bytes, "launch_ms": round(dec_avg, 4)},
+        "roofline": ({"bound": "tensor", "achieved": round(flops / (dec_avg * 1e-3) / 1e12, 1),
+                      "peak": tc_peak, "peak_source": f"{peak_src} bf16_tflops", "unit": "TFLOP/s",
+                      "frac": round(flops / (dec_avg * 1e-3) / 1e12 / tc_peak, 4), "traffic": None}
+                     if tensor_bound else
+                     {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                      "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
+                      "frac": round(achieved / hbm_peak, 4),
+                      "traffic": traffic_per_launch(cfg.name if not args.reqs else "", kv_bytes)}),
         "gpu_launches": launches_per_step * args.steps,
+        "roofline_detail": {"kernel": f"dcp_decode_{cfg.kind} (plan + split + merge)",
+                            "alg_bytes_per_launch": alg_bytes, "alg_flops_per_launch": flops,
+                            "launch_ms": round(dec_avg, 4),
+                            "roofline_ms": round(1e3 * max(t_hbm, t_tc), 4),
+                            "hbm_ms": round(1e3 * t_hbm, 4), "tensor_ms": round(1e3 * t_tc, 4),
+                            "tensor_tflops": round(flops / (dec_avg * 1e-3) / 1e12, 1)},
         "clocks": clocks,
         "setup_s": round(setup_s, 2),
     }

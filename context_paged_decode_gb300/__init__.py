@@ -69,6 +69,7 @@ def load(path: str = LIB_PATH):
         "dcp_cache_write_gqa": (C.c_int, [L, vp, vp, i64, i32, i32, C.c_int, vp, i64, RP, RP, vp,
                                           vp]),
         "dcp_cache_write_mla": (C.c_int, [L, vp, i64, i32, C.c_int, vp, i64, RP, vp, vp]),
+        "dcp_gather_context_mla": (C.c_int, [L, PK, i32, i32, C.c_int, vp, vp, i64, vp, vp, vp]),
         "dcp_decode_workspace_size": (C.c_int, [L, C.c_int, i32, i32, i32, i32,
                                                 C.POINTER(C.c_size_t)]),
         "dcp_decode_partial_gqa": (C.c_int, [L, vp, i32, i32, i32, i32, f32, C.c_int, PK, vp, vp,
@@ -99,7 +100,8 @@ def load(path: str = LIB_PATH):
 def exported_symbols():
     """Names of the C entry points this binding expects the library to export."""
     return ["dcp_strerror", "dcp_version", "dcp_local_seq_lens", "dcp_slot_mapping",
-            "dcp_cache_write_gqa", "dcp_cache_write_mla", "dcp_decode_workspace_size",
+            "dcp_cache_write_gqa", "dcp_cache_write_mla", "dcp_gather_context_mla",
+            "dcp_decode_workspace_size",
             "dcp_decode_partial_gqa", "dcp_lse_merge", "dcp_decode_gqa", "dcp_decode_gqa_noalloc",
             "dcp_decode_partial_mla",
             "dcp_decode_mla", "dcp_sfa_remap", "dcp_sfa_decode_partial", "dcp_sfa_decode"]
@@ -224,6 +226,22 @@ def cache_write_mla(layout, kv, slot, pools, num_blocks, err=None, stream=None):
     T, dk = kv.shape
     _check(lib.dcp_cache_write_mla(layout, _p(kv), T, dk, _dtype(kv), _p(slot), int(num_blocks),
                                    rank_ptrs(pools), _p(err), _stream(stream)))
+
+
+def gather_context_mla(layout, kv: PagedKV, req_idx, positions, out=None, err=None,
+                       stream=None):
+    """Rows of tokens (req_idx[t], positions[t]) from the sharded latent cache."""
+    lib = load()
+    _cuda_contig(req_idx, positions)
+    T = req_idx.shape[0]
+    pool = kv.k_pools[0]
+    kv_dim = pool.shape[-1]
+    B = kv.block_table.shape[-2]
+    if out is None:
+        out = torch.empty((T, kv_dim), dtype=pool.dtype, device=pool.device)
+    _check(lib.dcp_gather_context_mla(layout, kv.struct(), B, kv_dim, _dtype(pool), _p(req_idx),
+                                      _p(positions), T, _p(out), _p(err), _stream(stream)))
+    return out
 
 
 def decode_workspace_size(layout, kind, num_reqs, num_q_heads, num_kv_heads, head_dim_v):

@@ -57,6 +57,48 @@ static int launch_cache_write(int nsrc, const void* s0, const void* s1, int64_t 
   return launch_status();
 }
 
+// Context gather: one warp per requested token resolves its owner rank and
+// slot once, then copies the row in 16-byte pieces.  Unresolvable tokens get
+// a zero row and are counted.
+__global__ void gather_rows_kernel(Layout L, dcp_rank_ptrs_t pools, int64_t num_blocks,
+                                   const int32_t* __restrict__ bt, int B, int max_vb,
+                                   int64_t bt_rank_stride, const int32_t* __restrict__ req,
+                                   const int64_t* __restrict__ pos, int64_t T, int cpr,
+                                   uint4* __restrict__ out, int32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
+       t += nwarps) {
+    int owner = -1;
+    int64_t slot = -1;
+    if (lane == 0) {
+      const int b = req[t];
+      const int64_t x = pos[t];
+      if (b >= 0 && b < B && x >= 0) {
+        int r, loc;
+        int64_t vb;
+        place_token(x, L, r, vb, loc);
+        const int64_t phys =
+            vb < max_vb ? (int64_t)bt[r * bt_rank_stride + (int64_t)b * max_vb + vb] : -1;
+        if (phys >= 0 && phys < num_blocks) {
+          owner = r;
+          slot = phys * L.bs + loc;
+        }
+      }
+      if (owner < 0) count_error(err);
+    }
+    owner = __shfl_sync(0xffffffffu, owner, 0);
+    slot = __shfl_sync(0xffffffffu, slot, 0);
+    uint4* dst = out + t * cpr;
+    if (owner < 0) {
+      for (int c = lane; c < cpr; c += 32) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(pools.ptr[owner]) + slot * cpr;
+      for (int c = lane; c < cpr; c += 32) dst[c] = __ldg(src + c);
+    }
+  }
+}
+
 }  // namespace dcp
 
 using namespace dcp;
@@ -95,6 +137,27 @@ int dcp_cache_write_mla(dcp_layout_t layout, const void* kv, int64_t num_tokens,
   return launch_cache_write(1, kv, nullptr, num_tokens, 1, kv_dim * es, layout.block_size,
                             layout.dcp_size, slot, num_blocks, cache, cache, err_count,
                             (cudaStream_t)stream);
+}
+
+int dcp_gather_context_mla(dcp_layout_t layout, dcp_paged_kv_t kv, int32_t num_reqs,
+                           int32_t kv_dim, dcp_dtype_t dtype, const int32_t* req_idx,
+                           const int64_t* positions, int64_t num_tokens, void* out,
+                           int32_t* err_count, dcp_stream_t stream) {
+  const int es = elem_bytes(dtype);
+  if (!layout_ok(layout) || es == 0 || num_reqs < 0 || num_tokens < 0 || kv_dim < 1 ||
+      kv.num_blocks < 0 || kv.max_vblocks < 0 || kv.bt_rank_stride < 0)
+    return DCP_EINVAL;
+  if ((kv_dim * es) % 16 != 0) return DCP_EUNSUPPORTED;
+  if (num_tokens == 0) return DCP_OK;
+  if (!req_idx || !positions || !out || !kv.block_table || !ranks_ok(kv.k, layout.dcp_size))
+    return DCP_EINVAL;
+  const Layout L{layout.dcp_size, layout.block_size, layout.interleave};
+  const int64_t blocks = (num_tokens + 7) / 8;
+  const int grid = (int)(blocks < 16 * num_sms() ? blocks : 16 * num_sms());
+  gather_rows_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(
+      L, kv.k, kv.num_blocks, kv.block_table, num_reqs, kv.max_vblocks, kv.bt_rank_stride,
+      req_idx, positions, num_tokens, kv_dim * es / 16, (uint4*)out, err_count);
+  return launch_status();
 }
 
 }  // extern "C"

@@ -175,6 +175,27 @@ int dcp_cache_write_mla(dcp_layout_t layout, const void* kv, int64_t num_tokens,
                         dcp_rank_ptrs_t cache, int32_t* err_count, dcp_stream_t stream);
 
 /*
+ * dcp_gather_context_mla -- read tokens back out of the sharded latent cache
+ * in the order given, page "Decode Context Parallel (DCP)", section "Prefill
+ * and chunked prefill" (MLA gathers the context KV cache and restores
+ * request-contiguous order before attending it).  Passing every position
+ * 0..L_b-1 of request b, in order, restores that request's contiguous
+ * context.
+ *  kv          latent pools [num_blocks][block_size][kv_dim] + block table
+ *              (kv.v is ignored).
+ *  req_idx     [num_tokens] int32, positions [num_tokens] int64.
+ *  out         [num_tokens][kv_dim] of dtype: bytes copied unchanged.
+ * A token that does not resolve to a stored slot (request outside
+ * [0, num_reqs), negative position, virtual block beyond the table, table
+ * entry outside [0, num_blocks)) gets a zero row and bumps err_count.
+ * kv_dim * element size must be a multiple of 16 bytes.
+ */
+int dcp_gather_context_mla(dcp_layout_t layout, dcp_paged_kv_t kv, int32_t num_reqs,
+                           int32_t kv_dim, dcp_dtype_t dtype, const int32_t* req_idx,
+                           const int64_t* positions, int64_t num_tokens, void* out,
+                           int32_t* err_count, dcp_stream_t stream);
+
+/*
  * dcp_decode_workspace_size -- bytes of device workspace the decode calls
  * below need for a batch of this shape (an upper bound that holds for any
  * context lengths).  The caller allocates it; its contents need not be

@@ -275,3 +275,29 @@ def sfa_sharded(q, K_all, V_all, scale, sel, L, dcp, bs, I, sink=None):
         po[r], pl[r] = attention(q, K_all[mine], V_all[mine], scale)
     o, lse = lse_merge(po, pl, sink)
     return o, lse, po, pl
+
+
+# ---------------------------------------------------------------------------
+# chunked-prefill context gather ("Decode Context Parallel (DCP)", section
+# "Prefill and chunked prefill": MLA gathers the context KV cache and
+# restores request-contiguous order)
+# ---------------------------------------------------------------------------
+
+def gather_context(req, pos, caches, block_table, dcp, bs, I, num_blocks):
+    """Rows of tokens (req[t], pos[t]) read back from the per-rank caches.
+
+    caches[r]: token-major pool [num_blocks*bs, width] of rank r.  A token
+    whose slot cannot be resolved gives a zero row (and is reported in the
+    returned `bad` count).
+    """
+    rank, slot = slot_mapping(req, pos, block_table, None, dcp, bs, I, num_blocks)
+    width = caches[0].shape[1]
+    out = np.zeros((len(req), width), dtype=caches[0].dtype)
+    bad = 0
+    for t in range(len(req)):
+        r = int(rank[t])
+        if r < 0:
+            bad += 1
+            continue
+        out[t] = caches[r][int(slot[r, t])]
+    return out, bad

@@ -280,3 +280,25 @@ def test_sfa_remap_matches_slot_mapping_and_sparse_merge():
     o2, lse2 = O.sparse_attention(q, K, V, 0.4, topk[0])
     np.testing.assert_allclose(o, o2, rtol=1e-12)
     assert lse == pytest.approx(lse2, rel=1e-13)
+
+
+def test_gather_context_inverts_the_cache_write():
+    import workloads as W
+    for dcp, bs, I in [(2, 4, 2), (4, 16, 1), (3, 8, 8)]:
+        lens = np.array([1, 50, 3 * bs * dcp + 7])
+        bt, nb = W.make_block_tables(lens, dcp, bs, "random", seed=dcp)
+        req = np.concatenate([np.full(L, b) for b, L in enumerate(lens)])
+        pos = np.concatenate([np.arange(L) for L in lens])
+        rows = np.arange(len(req) * 3).reshape(len(req), 3) + 7
+        _, slot = O.slot_mapping(req, pos, bt, lens, dcp, bs, I, nb)
+        caches = O.build_caches(rows, slot, dcp, nb, bs, -1)
+        # request-contiguous order is the write order: the gather returns the rows
+        out, bad = O.gather_context(req, pos, caches, bt, dcp, bs, I, nb)
+        assert bad == 0 and (out == rows).all()
+        # any other order of tokens gives the same rows permuted
+        perm = np.random.default_rng(1).permutation(len(req))
+        out, _ = O.gather_context(req[perm], pos[perm], caches, bt, dcp, bs, I, nb)
+        assert (out == rows[perm]).all()
+        # unresolvable tokens give zero rows
+        out, bad = O.gather_context([0, 5], [10 ** 6, 0], caches, bt, dcp, bs, I, nb)
+        assert bad == 2 and (out == 0).all()
