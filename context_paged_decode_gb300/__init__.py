@@ -75,6 +75,8 @@ def load(path: str = LIB_PATH):
         "dcp_decode_partial_gqa": (C.c_int, [L, vp, i32, i32, i32, i32, f32, C.c_int, PK, vp, vp,
                                              vp, vp, C.c_size_t, vp, vp]),
         "dcp_lse_merge": (C.c_int, [i32, vp, vp, i32, i32, i32, vp, vp, C.c_int, vp, vp]),
+        "dcp_lse_merge_swa": (C.c_int, [i32, vp, vp, vp, vp, i32, i32, i32, vp, vp, C.c_int, vp,
+                                        vp]),
         "dcp_decode_gqa": (C.c_int, [L, vp, i32, i32, i32, i32, f32, C.c_int, PK, vp, vp, vp,
                                      C.c_int, vp, vp, C.c_size_t, vp, vp]),
         "dcp_decode_gqa_noalloc": (C.c_int, [L, vp, i32, i32, i32, i32, f32, C.c_int, PK, vp, vp,
@@ -84,6 +86,9 @@ def load(path: str = LIB_PATH):
         "dcp_decode_mla": (C.c_int, [L, vp, i32, i32, i32, i32, f32, C.c_int, PK, vp, vp, vp,
                                      C.c_int, vp, vp, C.c_size_t, vp, vp]),
         "dcp_sfa_remap": (C.c_int, [L, vp, i32, i32, vp, vp, i32, i64, i64, vp, vp, vp, vp]),
+        "dcp_sfa_compact_workspace_size": (C.c_int, [L, i64, C.POINTER(C.c_size_t)]),
+        "dcp_sfa_compact_blocks": (C.c_int, [L, vp, vp, i32, i32, vp, i32, PK, i32, C.c_int, i64,
+                                             vp, vp, vp, vp, vp, C.c_size_t, vp, vp]),
         "dcp_sfa_decode_partial": (C.c_int, [L, vp, i32, i32, i32, i32, f32, C.c_int, PK, vp, vp,
                                              i32, vp, vp, vp, vp]),
         "dcp_sfa_decode": (C.c_int, [L, vp, i32, i32, i32, i32, f32, C.c_int, PK, vp, i32, vp, vp,
@@ -102,9 +107,11 @@ def exported_symbols():
     return ["dcp_strerror", "dcp_version", "dcp_local_seq_lens", "dcp_slot_mapping",
             "dcp_cache_write_gqa", "dcp_cache_write_mla", "dcp_gather_context_mla",
             "dcp_decode_workspace_size",
-            "dcp_decode_partial_gqa", "dcp_lse_merge", "dcp_decode_gqa", "dcp_decode_gqa_noalloc",
+            "dcp_decode_partial_gqa", "dcp_lse_merge", "dcp_lse_merge_swa", "dcp_decode_gqa",
+            "dcp_decode_gqa_noalloc",
             "dcp_decode_partial_mla",
-            "dcp_decode_mla", "dcp_sfa_remap", "dcp_sfa_decode_partial", "dcp_sfa_decode"]
+            "dcp_decode_mla", "dcp_sfa_remap", "dcp_sfa_compact_workspace_size", "dcp_sfa_compact_blocks",
+            "dcp_sfa_decode_partial", "dcp_sfa_decode"]
 
 
 def _check(rc):
@@ -332,6 +339,22 @@ def lse_merge(part_o, part_lse, sink=None, out_dtype=torch.float32, out=None, ou
     return out, out_lse
 
 
+def lse_merge_swa(part_o, part_lse, swa_o, swa_lse, sink=None, out_dtype=torch.float32, out=None,
+                  out_lse=None, stream=None):
+    """Merge the per-rank partials with ONE replicated-window partial (+ sink)."""
+    lib = load()
+    _cuda_contig(part_o, part_lse, swa_o, swa_lse, sink)
+    n, B, H, dv = part_o.shape
+    dev = part_o.device
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=out_dtype, device=dev)
+    if out_lse is None:
+        out_lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    _check(lib.dcp_lse_merge_swa(n, _p(part_o), _p(part_lse), _p(swa_o), _p(swa_lse), B, H, dv,
+                                 _p(sink), _p(out), _dtype(out), _p(out_lse), _stream(stream)))
+    return out, out_lse
+
+
 def decode_partial_mla(layout, q, kv: PagedKV, local_lens, scale, v_dim=512, part_o=None,
                        part_lse=None, workspace=None, err=None, stream=None):
     lib = load()
@@ -384,6 +407,29 @@ def sfa_remap(layout, topk, seq_lens, block_table, num_blocks, out_rank=None, ou
                              stride, int(num_blocks), _p(out_rank), _p(out_slot), _p(err),
                              _stream(stream)))
     return out_rank, out_slot
+
+
+def sfa_compact_blocks(layout, kv: PagedKV, topk, q_req, seq_lens, max_blocks, err=None,
+                       stream=None):
+    """Compact the referenced latent blocks; returns (blocks, ids, counts, index)."""
+    lib = load()
+    _cuda_contig(topk, q_req, seq_lens)
+    Q, K = topk.shape
+    pool = kv.k_pools[0]
+    kv_dim, bs = pool.shape[-1], pool.shape[-2]
+    dev = pool.device
+    n = C.c_size_t(0)
+    _check(lib.dcp_sfa_compact_workspace_size(layout, kv.num_blocks, C.byref(n)))
+    ws = torch.empty(max(n.value, 1), dtype=torch.uint8, device=dev)
+    blocks = torch.empty((max(max_blocks, 1), bs, kv_dim), dtype=pool.dtype, device=dev)
+    ids = torch.empty(max(max_blocks, 1), dtype=torch.int32, device=dev)
+    counts = torch.empty(layout.dcp_size, dtype=torch.int32, device=dev)
+    index = torch.empty((Q, K), dtype=torch.int64, device=dev)
+    _check(lib.dcp_sfa_compact_blocks(layout, _p(topk), _p(q_req), Q, K, _p(seq_lens),
+                                      kv.block_table.shape[-2], kv.struct(), kv_dim, _dtype(pool),
+                                      int(max_blocks), _p(blocks), _p(ids), _p(counts),
+                                      _p(index), _p(ws), ws.numel(), _p(err), _stream(stream)))
+    return blocks, ids, counts, index
 
 
 def sfa_decode_partial(layout, q, kv: PagedKV, sel_rank, sel_slot, scale, v_dim=512,

@@ -20,6 +20,21 @@ struct DenseParts {  // part_o [n][B][H][dv], part_lse [n][B][H]
   }
 };
 
+struct DensePlusOne {  // n dense parts [n][B][H][dv] and one more part [B][H][dv]
+  const float* o;
+  const float* lse;
+  int64_t stride;  // B*H
+  int n;
+  const float* xo;
+  const float* xlse;
+  __device__ __forceinline__ float lse_at(int i, int64_t row) const {
+    return i < n ? lse[i * stride + row] : xlse[row];
+  }
+  __device__ __forceinline__ const float* o_at(int i, int64_t row, int dv) const {
+    return i < n ? o + (i * stride + row) * dv : xo + row * dv;
+  }
+};
+
 struct ItemParts {  // plan items: lse [item][G], o [item][G][dv]
   const float* o;
   const float* lse;
@@ -119,6 +134,21 @@ __global__ void dense_merge_kernel(int n, const float* __restrict__ po,
                 out_lse);
 }
 
+template <int CH>
+__global__ void dense_plus_one_merge_kernel(int n, const float* __restrict__ po,
+                                            const float* __restrict__ pl,
+                                            const float* __restrict__ xo,
+                                            const float* __restrict__ xl, int B, int H, int dv,
+                                            const float* __restrict__ sink, void* out,
+                                            int out_dtype, float* out_lse) {
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= (int64_t)B * H) return;
+  const int h = (int)(row % H);
+  DensePlusOne P{po, pl, (int64_t)B * H, n, xo, xl};
+  merge_row<CH>(P, n + 1, row, dv, sink != nullptr, sink ? sink[h] : 0.f, out, out_dtype, row,
+                out_lse);
+}
+
 // mode 0: row = (b, h), parts = all items of (b, g) over every rank; sink applies.
 // mode 1: row = (r, b, h), parts = items of (b, g, r); output is float32 per rank.
 template <int CH>
@@ -198,5 +228,36 @@ extern "C" int dcp_lse_merge(int32_t num_parts, const float* part_o, const float
     dense_merge_kernel<8><<<grid, wpb * 32, 0, st>>>(num_parts, part_o, part_lse, num_reqs,
                                                      num_heads, head_dim_v, sink, out,
                                                      (int)out_dtype, out_lse);
+  return launch_status();
+}
+
+extern "C" int dcp_lse_merge_swa(int32_t num_parts, const float* part_o, const float* part_lse,
+                                 const float* swa_o, const float* swa_lse, int32_t num_reqs,
+                                 int32_t num_heads, int32_t head_dim_v, const float* sink,
+                                 void* out, dcp_dtype_t out_dtype, float* out_lse,
+                                 dcp_stream_t stream) {
+  if (num_parts < 0 || num_reqs < 0 || num_heads < 0 || head_dim_v < 4 || head_dim_v % 4 != 0 ||
+      head_dim_v > 1024 || (out_dtype != DCP_F32 && out_dtype != DCP_BF16))
+    return DCP_EINVAL;
+  const int64_t rows = (int64_t)num_reqs * num_heads;
+  if (rows == 0) return DCP_OK;
+  if (!out || !swa_o || !swa_lse || (num_parts > 0 && (!part_o || !part_lse))) return DCP_EINVAL;
+  const int wpb = 8;
+  const unsigned grid = (unsigned)((rows + wpb - 1) / wpb);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int nv = head_dim_v / 4;
+#define DCP_MERGE_SWA(CH)                                                                  \
+  dense_plus_one_merge_kernel<CH><<<grid, wpb * 32, 0, st>>>(                              \
+      num_parts, part_o, part_lse, swa_o, swa_lse, num_reqs, num_heads, head_dim_v, sink, \
+      out, (int)out_dtype, out_lse)
+  if (nv <= 32)
+    DCP_MERGE_SWA(1);
+  else if (nv <= 64)
+    DCP_MERGE_SWA(2);
+  else if (nv <= 128)
+    DCP_MERGE_SWA(4);
+  else
+    DCP_MERGE_SWA(8);
+#undef DCP_MERGE_SWA
   return launch_status();
 }

@@ -256,6 +256,24 @@ int dcp_lse_merge(int32_t num_parts, const float* part_o, const float* part_lse,
                   void* out, dcp_dtype_t out_dtype, float* out_lse, dcp_stream_t stream);
 
 /*
+ * dcp_lse_merge_swa -- dcp_lse_merge with one more part: the partial of a
+ * sliding-window (SWA) KV set that every rank holds in full.  Page
+ * "DeepSeek V4.1 context parallelism", section "Decode computation":
+ * replicated SWA contributes on one rank, and the sink is applied once when
+ * the partials are merged by log-sum-exp.  The window partial is therefore
+ * merged exactly once, next to the num_parts per-rank partials:
+ *     lse = ln( sum_i exp(lse_i) + exp(swa_lse) + exp(sink[h]) ).
+ *  swa_o   [num_reqs][num_heads][head_dim_v] float32, swa_lse
+ *          [num_reqs][num_heads] float32 (-inf = empty window), e.g. from
+ *          dcp_decode_partial_gqa with dcp_size 1 over the window cache.
+ * Other arguments as for dcp_lse_merge.
+ */
+int dcp_lse_merge_swa(int32_t num_parts, const float* part_o, const float* part_lse,
+                      const float* swa_o, const float* swa_lse, int32_t num_reqs,
+                      int32_t num_heads, int32_t head_dim_v, const float* sink, void* out,
+                      dcp_dtype_t out_dtype, float* out_lse, dcp_stream_t stream);
+
+/*
  * dcp_decode_gqa -- the fused decode step: per-rank split-KV partials and
  * one merge over (rank x split) with the optional sink, giving the same
  * result as dcp_decode_partial_gqa followed by dcp_lse_merge.
@@ -343,6 +361,42 @@ int dcp_sfa_remap(dcp_layout_t layout, const int32_t* topk, int32_t num_reqs, in
                   const int32_t* seq_lens, const int32_t* block_table, int32_t max_vblocks,
                   int64_t bt_rank_stride, int64_t num_blocks, int32_t* out_rank,
                   int32_t* out_slot, int32_t* err_count, dcp_stream_t stream);
+
+/*
+ * dcp_sfa_compact_workspace_size -- bytes of workspace dcp_sfa_compact_blocks
+ * needs for pools of num_blocks physical blocks per rank.
+ */
+int dcp_sfa_compact_workspace_size(dcp_layout_t layout, int64_t num_blocks, size_t* bytes);
+
+/*
+ * dcp_sfa_compact_blocks -- page "Decode Context Parallel (DCP)", section
+ * "GLM-5.2 SFA DCP replicated indexer": during prefill or a mixed batch only
+ * the KV blocks referenced by the sparse block table are compacted (and then
+ * all-gathered after the layer writes its KV cache).  This is the one-GPU
+ * part: every rank's physical blocks that some selected token of some query
+ * refers to are numbered (ranks in order, increasing block id within a
+ * rank), copied into one buffer, and every selected token is rewritten as a
+ * row of that buffer.
+ *  topk       [num_queries][topk_len] int32 global token ids (index < 0 or
+ *             >= seq_lens[q_req[q]] is padding: skipped, index -1).
+ *  q_req      [num_queries] int32 request of each query.
+ *  kv         latent pools [num_blocks][block_size][kv_dim] + block table.
+ *  out_blocks [max_blocks][block_size][kv_dim] of dtype: the compacted blocks.
+ *  out_block_ids [max_blocks] int32 physical id of each compacted block.
+ *  out_counts [dcp_size] int32 compacted blocks of each rank (their sum may
+ *             exceed max_blocks: blocks past the capacity are not stored and
+ *             the tokens in them get index -1 and bump err_count).
+ *  out_index  [num_queries][topk_len] int64 row of each selected token in
+ *             out_blocks viewed as [max_blocks*block_size][kv_dim], or -1.
+ *  workspace  dcp_sfa_compact_workspace_size bytes (contents not needed).
+ * A table entry outside [0, num_blocks) gives -1 and bumps err_count.
+ */
+int dcp_sfa_compact_blocks(dcp_layout_t layout, const int32_t* topk, const int32_t* q_req,
+                           int32_t num_queries, int32_t topk_len, const int32_t* seq_lens,
+                           int32_t num_reqs, dcp_paged_kv_t kv, int32_t kv_dim, dcp_dtype_t dtype,
+                           int64_t max_blocks, void* out_blocks, int32_t* out_block_ids,
+                           int32_t* out_counts, int64_t* out_index, void* workspace,
+                           size_t workspace_bytes, int32_t* err_count, dcp_stream_t stream);
 
 /*
  * dcp_sfa_decode_partial -- per-rank sparse attention over the selected

@@ -278,6 +278,61 @@ def sfa_sharded(q, K_all, V_all, scale, sel, L, dcp, bs, I, sink=None):
 
 
 # ---------------------------------------------------------------------------
+# SFA prefill compaction ("Decode Context Parallel (DCP)", section "GLM-5.2
+# SFA DCP replicated indexer": during prefill or a mixed batch, only the KV
+# blocks referenced by the sparse block table are compacted, then gathered)
+# ---------------------------------------------------------------------------
+
+def sfa_compact_blocks(topk, q_req, seq_lens, block_table, caches, dcp, bs, I, num_blocks):
+    """Reference compaction.
+
+    topk[Q, K] global token ids of each query, q_req[Q] its request.
+    Returns (blocks [n, bs, width] copied from the per-rank caches -- ranks
+    in order, each rank's referenced physical blocks in increasing id
+    order --, ids [n] physical id of each, counts [dcp], index [Q, K] row of
+    each selected token in blocks viewed as [n*bs, width], -1 when invalid).
+    caches[r] is rank r's token-major pool [num_blocks*bs, width].
+    """
+    Q, K = topk.shape
+    refs = [set() for _ in range(dcp)]
+    where = np.full((Q, K, 2), -1, dtype=np.int64)  # (rank, phys*bs + loc) per entry
+    for qi in range(Q):
+        b = int(q_req[qi])
+        for k in range(K):
+            g = int(topk[qi, k])
+            if b < 0 or b >= len(seq_lens) or g < 0 or g >= int(seq_lens[b]):
+                continue
+            vb = virtual_block_index(g, bs, dcp)
+            if vb >= block_table.shape[2]:
+                continue
+            r = target_rank(g, bs, dcp, I)
+            phys = int(block_table[r, b, vb])
+            if phys < 0 or phys >= num_blocks:
+                continue
+            refs[r].add(phys)
+            where[qi, k] = (r, phys * bs + local_offset(g, bs, dcp, I))
+    ids, counts, first = [], [], {}
+    for r in range(dcp):
+        srt = sorted(refs[r])
+        counts.append(len(srt))
+        for p in srt:
+            first[(r, p)] = len(ids)
+            ids.append(p)
+    width = caches[0].shape[1]
+    blocks = np.zeros((len(ids), bs, width), dtype=caches[0].dtype)
+    for r in range(dcp):
+        for p in sorted(refs[r]):
+            blocks[first[(r, p)]] = caches[r][p * bs:(p + 1) * bs]
+    index = np.full((Q, K), -1, dtype=np.int64)
+    for qi in range(Q):
+        for k in range(K):
+            r, s = where[qi, k]
+            if r >= 0:
+                index[qi, k] = first[(int(r), int(s) // bs)] * bs + int(s) % bs
+    return blocks, np.asarray(ids, dtype=np.int64), np.asarray(counts, dtype=np.int64), index
+
+
+# ---------------------------------------------------------------------------
 # chunked-prefill context gather ("Decode Context Parallel (DCP)", section
 # "Prefill and chunked prefill": MLA gathers the context KV cache and
 # restores request-contiguous order)

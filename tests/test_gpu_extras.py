@@ -54,6 +54,68 @@ def test_gather_context_full_size_longest_request(lib):
     assert (out.view(torch.int16).cpu().numpy() == want).all()
 
 
+@pytest.mark.parametrize("dcp_size,bs,I,cap", [(8, 64, 64, None), (4, 16, 1, None), (3, 8, 8, 5)])
+def test_sfa_compaction_matches_oracle(lib, dcp_size, bs, I, cap):
+    import oracle as O
+    cfg = dataclasses.replace(W.CONFIGS["sfa_bf16_b32"], B=2, lengths=[5000, 700], dcp=dcp_size, topk=64,
+                              bs=bs, I=I)
+    wl = D.build(cfg)
+    rng = np.random.default_rng(dcp_size)
+    q_req = np.array([0, 1, 0, 0, 1], dtype=np.int32)
+    topk = np.stack([rng.choice(int(wl.seq_lens_host[b]), 64, replace=False) for b in q_req])
+    topk = topk.astype(np.int32)
+    topk[1, :2] = [-1, 700]                      # padding entries
+    # reference caches from the generator rows (bit patterns)
+    lens = wl.seq_lens_host
+    req = np.concatenate([np.full(int(L), b) for b, L in enumerate(lens)])
+    pos = np.concatenate([np.arange(int(L)) for L in lens])
+    rows = np.concatenate([W.token_rows(cfg, W.T_LATENT, b, 0, int(L)) for b, L in enumerate(lens)])
+    _, slot = O.slot_mapping(req, pos, wl.bt_host, lens, cfg.dcp, cfg.bs, cfg.I, wl.num_blocks)
+    caches = O.build_caches(rows.view(np.int16), slot, cfg.dcp, wl.num_blocks, cfg.bs, -1)
+    eb, eids, ecounts, eindex = O.sfa_compact_blocks(topk, q_req, lens, wl.bt_host, caches,
+                                                     cfg.dcp, cfg.bs, cfg.I, wl.num_blocks)
+    max_blocks = len(eids) if cap is None else cap
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    blocks, ids, counts, index = lib.sfa_compact_blocks(
+        wl.layout, wl.kv, torch.from_numpy(topk).cuda(), torch.from_numpy(q_req).cuda(),
+        wl.seq_lens, max_blocks, err=err)
+    counts = counts.cpu().numpy()
+    assert (counts == ecounts).all()
+    n = min(max_blocks, len(eids))
+    assert (ids.cpu().numpy()[:n] == eids[:n]).all()
+    got_blocks = blocks.view(torch.int16).cpu().numpy()[:n]
+    assert (got_blocks == eb[:n]).all()
+    idx = index.cpu().numpy()
+    want = np.where(eindex < n * cfg.bs, eindex, -1)
+    assert (idx == want).all()
+    assert err.item() == int(((eindex >= n * cfg.bs)).sum())
+
+
+def test_replicated_window_merged_once(lib):
+    """Sharded global KV (dcp=4) + a sliding window every rank holds in full
+    (computed once, as a dcp=1 partial) + sink, merged by dcp_lse_merge_swa."""
+    import oracle as O
+    glob = dataclasses.replace(W.CONFIGS["gqa_bf16_b32"], B=3, lengths=[3000, 40, 900], dcp=4)
+    win = dataclasses.replace(glob, lengths=[128, 7, 128], dcp=1, bs=16, I=1, seed=77)
+    wg, ww = D.build(glob), D.build(win)
+    ww.q.copy_(wg.q)  # the same query attends both key sets
+    po, pl = lib.decode_partial_gqa(wg.layout, wg.q, wg.kv, wg.local_lens, glob.scale)
+    so, sl = lib.decode_partial_gqa(ww.layout, ww.q, ww.kv, ww.local_lens, win.scale)
+    sink = torch.from_numpy(np.linspace(-1, 2, glob.Hq).astype(np.float32)).cuda()
+    out, lse = lib.lse_merge_swa(po, pl, so[0].contiguous(), sl[0].contiguous(), sink)
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    s_host = sink.cpu().numpy()
+    G = glob.Hq // glob.Hkv
+    for b in range(glob.B):
+        for h in (0, 9, 31):
+            exp = ref.gqa_expected(glob, wg.seq_lens_host, b, [h])[h]
+            Kw, Vw = ref.gqa_kv(win, b, h // G, int(ww.seq_lens_host[b]))
+            ow, lw = O.attention(ref.q_vec(glob, b, h), Kw, Vw, glob.scale)
+            o_ref, lse_ref = O.lse_merge(np.vstack([exp[2], ow]), list(exp[3]) + [lw],
+                                         sink=float(s_host[h]))
+            ref.check_bf16(out[b, h], lse[b, h], o_ref, lse_ref, f"b{b} h{h}")
+
+
 # ---------------------------------------------------------------------------
 # graph capture: static launch parameters, lengths read from device memory
 # ---------------------------------------------------------------------------

@@ -282,6 +282,69 @@ def test_sfa_remap_matches_slot_mapping_and_sparse_merge():
     assert lse == pytest.approx(lse2, rel=1e-13)
 
 
+def test_replicated_window_contributes_once():
+    """'Replicated SWA contributes on one rank' (TokenSpeed page, "Decode
+    computation"): merging the per-rank partials of the sharded keys with
+    ONE partial of the replicated window keys (and the sink) equals attention
+    over the union of both key sets plus the sink key; adding the window
+    partial once per rank does not."""
+    rng = np.random.default_rng(8)
+    L, W, dcp, bs, I = 300, 40, 4, 8, 2
+    q, K, V = rnd(rng, 16), rnd(rng, L, 16), rnd(rng, L, 12)
+    Kw, Vw = rnd(rng, W, 16), rnd(rng, W, 12)
+    sigma, scale = 0.9, 0.3
+    _, _, po, pl = O.sharded_attention(q, K, V, scale, L, dcp, bs, I)
+    ow, lw = O.attention(q, Kw, Vw, scale)
+    o, lse = O.lse_merge(np.vstack([po, ow]), list(pl) + [lw], sink=sigma)
+    k_star = q * sigma / (scale * float(np.dot(q, q)))
+    o2, lse2 = O.attention(q, np.vstack([K, Kw, k_star]), np.vstack([V, Vw, np.zeros(12)]), scale)
+    np.testing.assert_allclose(o, o2, rtol=1e-11, atol=1e-13)
+    assert lse == pytest.approx(lse2, rel=1e-13)
+    o3, lse3 = O.lse_merge(np.vstack([po] + [ow] * dcp), list(pl) + [lw] * dcp, sink=sigma)
+    assert abs(lse3 - lse) > 1e-6
+
+
+def test_sfa_compaction_keeps_exactly_the_referenced_rows():
+    import workloads as W
+    dcp, bs, I = 4, 8, 8
+    lens = np.array([500, 90])
+    bt, nb = W.make_block_tables(lens, dcp, bs, "random", seed=4)
+    req = np.concatenate([np.full(L, b) for b, L in enumerate(lens)])
+    pos = np.concatenate([np.arange(L) for L in lens])
+    rows = np.arange(len(req) * 2).reshape(len(req), 2) + 1
+    _, slot = O.slot_mapping(req, pos, bt, lens, dcp, bs, I, nb)
+    caches = O.build_caches(rows, slot, dcp, nb, bs, -1)
+    rng = np.random.default_rng(5)
+    q_req = np.array([0, 0, 1, 0, 1])
+    topk = np.stack([rng.choice(int(lens[b]), 20, replace=False) for b in q_req])
+    topk[1, 3] = -1
+    topk[2, 0] = 90
+    blocks, ids, counts, index = O.sfa_compact_blocks(topk, q_req, lens, bt, caches, dcp, bs, I,
+                                                      nb)
+    flat = blocks.reshape(-1, 2)
+    for qi in range(len(q_req)):
+        for k in range(20):
+            g = int(topk[qi, k])
+            if g < 0 or g >= lens[q_req[qi]]:
+                assert index[qi, k] == -1
+                continue
+            t = int(np.nonzero((req == q_req[qi]) & (pos == g))[0][0])
+            assert (flat[index[qi, k]] == rows[t]).all()   # the selected token's own row
+    # exactly the referenced blocks: brute-force set of (rank, block) over entries
+    want = set()
+    for qi in range(len(q_req)):
+        for g in topk[qi]:
+            if 0 <= g < lens[q_req[qi]]:
+                r = O.target_rank(int(g), bs, dcp, I)
+                want.add((r, int(bt[r, q_req[qi], O.virtual_block_index(int(g), bs, dcp)])))
+    assert counts.sum() == len(want) == len(ids)
+    start = 0
+    for r in range(dcp):
+        got = list(ids[start:start + counts[r]])
+        assert got == sorted(p for rr, p in want if rr == r)
+        start += counts[r]
+
+
 def test_gather_context_inverts_the_cache_write():
     import workloads as W
     for dcp, bs, I in [(2, 4, 2), (4, 16, 1), (3, 8, 8)]:
