@@ -86,6 +86,10 @@ def load(path: str = LIB_PATH):
         "dcp_decode_mla": (C.c_int, [L, vp, i32, i32, i32, i32, f32, C.c_int, PK, vp, vp, vp,
                                      C.c_int, vp, vp, C.c_size_t, vp, vp]),
         "dcp_sfa_remap": (C.c_int, [L, vp, i32, i32, vp, vp, i32, i64, i64, vp, vp, vp, vp]),
+        "dcp_topk_workspace_size": (C.c_int, [L, i32, i32, C.POINTER(C.c_size_t)]),
+        "dcp_topk_local": (C.c_int, [L, vp, i32, i32, vp, i32, vp, vp]),
+        "dcp_topk_merge": (C.c_int, [i32, vp, i32, i32, vp, C.c_size_t, vp, vp, vp]),
+        "dcp_topk": (C.c_int, [L, vp, i32, i32, vp, i32, vp, vp, vp, C.c_size_t, vp]),
         "dcp_sfa_compact_workspace_size": (C.c_int, [L, i64, C.POINTER(C.c_size_t)]),
         "dcp_sfa_compact_blocks": (C.c_int, [L, vp, vp, i32, i32, vp, i32, PK, i32, C.c_int, i64,
                                              vp, vp, vp, vp, vp, C.c_size_t, vp, vp]),
@@ -110,7 +114,8 @@ def exported_symbols():
             "dcp_decode_partial_gqa", "dcp_lse_merge", "dcp_lse_merge_swa", "dcp_decode_gqa",
             "dcp_decode_gqa_noalloc",
             "dcp_decode_partial_mla",
-            "dcp_decode_mla", "dcp_sfa_remap", "dcp_sfa_compact_workspace_size", "dcp_sfa_compact_blocks",
+            "dcp_decode_mla", "dcp_sfa_remap", "dcp_topk_workspace_size", "dcp_topk_local", "dcp_topk_merge",
+            "dcp_topk", "dcp_sfa_compact_workspace_size", "dcp_sfa_compact_blocks",
             "dcp_sfa_decode_partial", "dcp_sfa_decode"]
 
 
@@ -407,6 +412,47 @@ def sfa_remap(layout, topk, seq_lens, block_table, num_blocks, out_rank=None, ou
                              stride, int(num_blocks), _p(out_rank), _p(out_slot), _p(err),
                              _stream(stream)))
     return out_rank, out_slot
+
+
+def topk_local(layout, local_scores, local_lens, k, cand=None, stream=None):
+    """Per-rank top-k candidate keys [dcp, B, k] (uint64 stored as int64)."""
+    lib = load()
+    _cuda_contig(local_scores, local_lens)
+    dcp_, B, max_local = local_scores.shape
+    if cand is None:
+        cand = torch.empty((dcp_, B, k), dtype=torch.int64, device=local_scores.device)
+    _check(lib.dcp_topk_local(layout, _p(local_scores), B, max_local, _p(local_lens), k, _p(cand),
+                              _stream(stream)))
+    return cand
+
+
+def topk_merge(cand, stream=None):
+    lib = load()
+    _cuda_contig(cand)
+    dcp_, B, k = cand.shape
+    dev = cand.device
+    ws = torch.empty(B * k * 8, dtype=torch.uint8, device=dev)
+    ids = torch.empty((B, k), dtype=torch.int32, device=dev)
+    scores = torch.empty((B, k), dtype=torch.float32, device=dev)
+    _check(lib.dcp_topk_merge(dcp_, _p(cand), B, k, _p(ws), ws.numel(), _p(ids), _p(scores),
+                              _stream(stream)))
+    return ids, scores
+
+
+def topk(layout, local_scores, local_lens, k, stream=None):
+    """Exact global top-k ids and scores [B, k] from per-rank local scores."""
+    lib = load()
+    _cuda_contig(local_scores, local_lens)
+    dcp_, B, max_local = local_scores.shape
+    dev = local_scores.device
+    n = C.c_size_t(0)
+    _check(lib.dcp_topk_workspace_size(layout, B, k, C.byref(n)))
+    ws = torch.empty(max(n.value, 1), dtype=torch.uint8, device=dev)
+    ids = torch.empty((B, k), dtype=torch.int32, device=dev)
+    scores = torch.empty((B, k), dtype=torch.float32, device=dev)
+    _check(lib.dcp_topk(layout, _p(local_scores), B, max_local, _p(local_lens), k, _p(ids),
+                        _p(scores), _p(ws), ws.numel(), _stream(stream)))
+    return ids, scores
 
 
 def sfa_compact_blocks(layout, kv: PagedKV, topk, q_req, seq_lens, max_blocks, err=None,

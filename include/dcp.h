@@ -363,6 +363,41 @@ int dcp_sfa_remap(dcp_layout_t layout, const int32_t* topk, int32_t num_reqs, in
                   int32_t* out_slot, int32_t* err_count, dcp_stream_t stream);
 
 /*
+ * Exact distributed top-k -- page "DeepSeek V4.1 context parallelism",
+ * section "Decode computation": every rank computes local top-k candidates
+ * over the tokens it owns and the scores and logical ids are merged across
+ * ranks, which selects exactly the global top-k.  Rule (the page names
+ * none): a higher score ranks first, equal scores rank the smaller logical
+ * (global) token id first, NaN counts as -inf, -0 equals +0 (reported
+ * scores: NaN as -inf, -0 as +0).
+ *
+ * dcp_topk_local
+ *  local_scores [dcp_size][num_reqs][max_local] float32: score of local
+ *               position p of request b on rank r (read for p < local_lens[b][r]).
+ *  local_lens   [num_reqs][dcp_size] int32 (dcp_local_seq_lens).
+ *  cand_keys    [dcp_size][num_reqs][k] uint64 candidates, best first:
+ *               key = (order(score) << 32) | (0xFFFFFFFF - id) with order()
+ *               the monotone map of float32 onto uint32; 0 = no candidate.
+ * dcp_topk_merge
+ *  out_ids      [num_reqs][k] int32 global token ids, best first (-1 when a
+ *               request has fewer than k tokens).
+ *  out_scores   [num_reqs][k] float32 (NULL allowed; -inf past the end).
+ *  workspace    num_reqs*k*8 bytes.
+ * dcp_topk     both steps; workspace dcp_topk_workspace_size bytes.
+ * 1 <= k <= 4096.
+ */
+int dcp_topk_workspace_size(dcp_layout_t layout, int32_t num_reqs, int32_t k, size_t* bytes);
+int dcp_topk_local(dcp_layout_t layout, const float* local_scores, int32_t num_reqs,
+                   int32_t max_local, const int32_t* local_lens, int32_t k, uint64_t* cand_keys,
+                   dcp_stream_t stream);
+int dcp_topk_merge(int32_t dcp_size, const uint64_t* cand_keys, int32_t num_reqs, int32_t k,
+                   void* workspace, size_t workspace_bytes, int32_t* out_ids, float* out_scores,
+                   dcp_stream_t stream);
+int dcp_topk(dcp_layout_t layout, const float* local_scores, int32_t num_reqs, int32_t max_local,
+             const int32_t* local_lens, int32_t k, int32_t* out_ids, float* out_scores,
+             void* workspace, size_t workspace_bytes, dcp_stream_t stream);
+
+/*
  * dcp_sfa_compact_workspace_size -- bytes of workspace dcp_sfa_compact_blocks
  * needs for pools of num_blocks physical blocks per rank.
  */

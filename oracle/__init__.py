@@ -278,6 +278,46 @@ def sfa_sharded(q, K_all, V_all, scale, sel, L, dcp, bs, I, sink=None):
 
 
 # ---------------------------------------------------------------------------
+# exact distributed top-k ("DeepSeek V4.1 context parallelism", section
+# "Decode computation": each rank computes local top-k candidates and the
+# scores and logical ids are merged across ranks -- exact top-k selection
+# under the kernel's score/tie rule)
+# ---------------------------------------------------------------------------
+# Rule (this library's, the page names none): a higher score ranks first; equal
+# scores rank the smaller logical (global) token id first; NaN counts as -inf.
+
+def _rank_order(scores, ids):
+    """Indices of (score, id) in rule order: higher score first, ties by
+    smaller id; NaN counts as -inf, and -0 and +0 are the same score."""
+    s = np.where(np.isnan(scores), -np.inf, np.asarray(scores, dtype=np.float64))
+    return np.lexsort((np.asarray(ids), -s))
+
+
+def topk_exact(scores, ids, k):
+    """Top-k of (score, id) pairs by the rule; returns (ids, scores) sorted."""
+    order = _rank_order(scores, ids)[:k]
+    return np.asarray(ids)[order], np.asarray(scores)[order]
+
+
+def topk_local(local_scores, local_len, r, k, dcp, bs, I):
+    """Rank r's candidates: the top-k of the scores of its local positions
+    (local position p holds global token global_token(p, r))."""
+    p = np.arange(int(local_len), dtype=np.int64)
+    ids = global_token(p, r, bs, dcp, I)
+    return topk_exact(np.asarray(local_scores)[:int(local_len)], ids, k)
+
+
+def topk_distributed(local_scores, local_lens, k, dcp, bs, I):
+    """Local top-k on every rank, then the top-k of all candidates."""
+    cand_ids, cand_scores = [], []
+    for r in range(dcp):
+        i, s = topk_local(local_scores[r], local_lens[r], r, k, dcp, bs, I)
+        cand_ids.append(i)
+        cand_scores.append(s)
+    return topk_exact(np.concatenate(cand_scores), np.concatenate(cand_ids), k)
+
+
+# ---------------------------------------------------------------------------
 # SFA prefill compaction ("Decode Context Parallel (DCP)", section "GLM-5.2
 # SFA DCP replicated indexer": during prefill or a mixed batch, only the KV
 # blocks referenced by the sparse block table are compacted, then gathered)

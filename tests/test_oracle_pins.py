@@ -304,6 +304,33 @@ def test_replicated_window_contributes_once():
     assert abs(lse3 - lse) > 1e-6
 
 
+def test_distributed_topk_is_exact_and_follows_the_tie_rule():
+    import heapq
+    rng = np.random.default_rng(12)
+    for dcp, bs, I, L, k in [(4, 8, 2, 500, 37), (8, 64, 64, 3000, 256), (3, 16, 1, 50, 64),
+                             (2, 4, 4, 9, 9)]:
+        # coarse scores: many ties
+        g_scores = np.round(rng.standard_normal(L) * 2) / 2
+        g_scores[rng.random(L) < 0.02] = np.nan
+        ids = np.arange(L)
+        # brute force: pick k times the best remaining (max score, then min id)
+        pool = [(-(-np.inf if np.isnan(s) else s), int(i)) for s, i in zip(g_scores, ids)]
+        want = [i for _, i in heapq.nsmallest(k, pool)]
+        got_ids, got_scores = O.topk_exact(g_scores, ids, k)
+        assert list(got_ids) == want
+        # the same selection from per-rank local scores
+        local = [[] for _ in range(dcp)]
+        for x in range(L):
+            local[O.target_rank(x, bs, dcp, I)].append(g_scores[x])
+        lens = [len(v) for v in local]
+        d_ids, d_scores = O.topk_distributed(local, lens, k, dcp, bs, I)
+        assert list(d_ids) == want
+        np.testing.assert_array_equal(d_scores, g_scores[want])
+    # -0 and +0 are one score, and NaN ties with -inf; ties go by the smaller id
+    z_ids, _ = O.topk_exact(np.array([0.0, -0.0, np.nan, -np.inf, 0.0]), np.array([4, 1, 0, 2, 3]), 5)
+    assert list(z_ids) == [1, 3, 4, 0, 2]
+
+
 def test_sfa_compaction_keeps_exactly_the_referenced_rows():
     import workloads as W
     dcp, bs, I = 4, 8, 8
