@@ -24,8 +24,12 @@ inline bool ranks_ok(const dcp_rank_ptrs_t& p, int dcp) {
   return true;
 }
 
+// DCP_OK, or DCP_ECUDA if the last runtime call or launch failed (the error
+// text goes to stderr when the environment sets DCP_VERBOSE).
+int launch_status_report(cudaError_t e);
 inline int launch_status() {
-  return cudaGetLastError() == cudaSuccess ? DCP_OK : DCP_ECUDA;
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DCP_OK : launch_status_report(e);
 }
 
 int num_sms();  // SM count of the current device (cached per device)
@@ -93,13 +97,19 @@ constexpr float kLn2 = 0.6931471805599453f;
 //   int32 hdr[4]         n_items, chunk_tokens, item counter, stuck counter
 //   int32 off[B*G*dcp+1] first item of (b, g, r)
 //   int4  item[max_items] {b, g << 8 | r, p0, p1}
+//   int32 ipart[max_items]   run of each item (balanced-parts plans only)
+//   int32 pfirst[kMaxParts+1] first item of each run (balanced-parts plans only)
 //   float lse[max_items * heads_per_item]
 //   float o[max_items * heads_per_item * dv]
+
+constexpr int kMaxParts = 1024;
 
 struct Plan {
   int32_t* hdr;
   int32_t* off;
   int4* item;
+  int32_t* ipart;
+  int32_t* pfirst;
   float* lse;
   float* o;
   int max_items;
@@ -109,6 +119,8 @@ inline size_t plan_bytes(int entries, int max_items, int heads_per_item, int dv)
   size_t b = 256;
   b += align_up(sizeof(int32_t) * (size_t)(entries + 1), 256);
   b += align_up(sizeof(int4) * (size_t)max_items, 256);
+  b += align_up(sizeof(int32_t) * (size_t)max_items, 256);
+  b += align_up(sizeof(int32_t) * (size_t)(kMaxParts + 1), 256);
   b += align_up(sizeof(float) * (size_t)max_items * heads_per_item, 256);
   b += align_up(sizeof(float) * (size_t)max_items * heads_per_item * dv, 256);
   return b;
@@ -123,6 +135,10 @@ inline Plan plan_carve(void* ws, int entries, int max_items, int heads_per_item)
   c += align_up(sizeof(int32_t) * (size_t)(entries + 1), 256);
   p.item = (int4*)c;
   c += align_up(sizeof(int4) * (size_t)max_items, 256);
+  p.ipart = (int32_t*)c;
+  c += align_up(sizeof(int32_t) * (size_t)max_items, 256);
+  p.pfirst = (int32_t*)c;
+  c += align_up(sizeof(int32_t) * (size_t)(kMaxParts + 1), 256);
   p.lse = (float*)c;
   c += align_up(sizeof(float) * (size_t)max_items * heads_per_item, 256);
   p.o = (float*)c;
@@ -134,6 +150,14 @@ inline Plan plan_carve(void* ws, int entries, int max_items, int heads_per_item)
 // rounded up to `tile`; items never cross a rank.
 int launch_plan(const int32_t* local_lens, int B, int dcp, int G, int tile, int min_chunk,
                 int target_items, const Plan& plan, cudaStream_t s);
+
+// Balanced-parts plan (G = 1): the local ranges of all (b, r), concatenated in
+// (b, r) order, are cut into `parts` runs of about equal token count; a cut
+// inside a range falls on a multiple of `tile` positions.  Items are the
+// pieces between cuts, in (b, r) order; run k owns items
+// [pfirst[k], pfirst[k+1]).  At most B*dcp + parts - 1 items; 1 <= parts <= kMaxParts.
+int launch_plan_parts(const int32_t* local_lens, int B, int dcp, int tile, int parts,
+                      const Plan& plan, cudaStream_t s);
 
 // Largest item count the MLA plan can produce (sizes its workspace).
 int mla_max_items(int B, int dcp);

@@ -6,9 +6,17 @@
 // context parallelism" (TokenSpeed), section "Cache ownership".  Remap:
 // "Decode Context Parallel (DCP)", section "GLM-5.2 SFA DCP replicated
 // indexer".
+#include <stdio.h>
+#include <stdlib.h>
+
 #include "dcp_common.cuh"
 
 namespace dcp {
+
+int launch_status_report(cudaError_t e) {
+  if (getenv("DCP_VERBOSE")) fprintf(stderr, "libdcp: CUDA error %d: %s\n", (int)e, cudaGetErrorString(e));
+  return DCP_ECUDA;
+}
 
 int num_sms() {
   static int cache[64] = {0};
@@ -206,6 +214,115 @@ int launch_plan(const int32_t* local_lens, int B, int dcp, int G, int tile, int 
                 int target_items, const Plan& plan, cudaStream_t s) {
   plan_kernel<<<1, kPlanThreads, 0, s>>>(local_lens, B, dcp, G, tile, min_chunk, target_items,
                                          plan);
+  return launch_status();
+}
+
+// Exclusive block scan of one int64 per thread; *total gets the sum.
+__device__ __forceinline__ int64_t block_scan_excl_i64(int64_t v, int64_t* sh, int64_t* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int64_t s = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    sh[lane] = s;
+  }
+  __syncthreads();
+  const int64_t warp_prefix = w > 0 ? sh[w - 1] : 0;
+  *total = sh[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return warp_prefix + x - v;
+}
+
+// Balanced-parts plan: entry e = b*dcp + r owns the global token range
+// [S_e, S_e + len_e) of the concatenation; tile t of the entry starts at
+// S_e + t*tile and belongs to run floor((S_e + t*tile) / per), with per =
+// ceil(total / parts) rounded up to the tile (so consecutive tiles differ by
+// at most one run and no run boundary splits a tile).
+__global__ void __launch_bounds__(kPlanThreads)
+plan_parts_kernel(const int32_t* __restrict__ local_lens, int B, int dcp, int tile, int parts,
+                  Plan plan) {
+  __shared__ int64_t sh64[33];
+  __shared__ int sh[32];
+  const int n = B * dcp;
+  const int per_thr = (n + blockDim.x - 1) / blockDim.x;
+  const int e0 = min(n, (int)threadIdx.x * per_thr), e1 = min(n, e0 + per_thr);
+  int64_t mine = 0;
+  for (int e = e0; e < e1; ++e) mine += max(local_lens[e], 0);
+  int64_t tot;
+  const int64_t start0 = block_scan_excl_i64(mine, sh64, &tot);
+  int64_t per = (tot + parts - 1) / parts;
+  per = (per + tile - 1) / tile * tile;
+  if (per < tile) per = tile;
+  // pieces of each entry: runs kf..kl of its first and last tile
+  int cnt = 0;
+  {
+    int64_t S = start0;
+    for (int e = e0; e < e1; ++e) {
+      const int64_t len = max(local_lens[e], 0);
+      if (len > 0) {
+        const int64_t last = S + (len - 1) / tile * tile;
+        cnt += (int)(last / per - S / per + 1);
+      }
+      S += len;
+    }
+  }
+  int total;
+  int base = block_scan_excl(cnt, sh, &total);
+  if (total > plan.max_items) total = plan.max_items;  // cannot happen with the sized bound
+  {
+    int64_t S = start0;
+    for (int e = e0; e < e1; ++e) {
+      const int64_t len = max(local_lens[e], 0);
+      plan.off[e] = min(base, plan.max_items);
+      if (len > 0) {
+        const int64_t ntiles = (len + tile - 1) / tile;
+        const int64_t kf = S / per, kl = (S + (ntiles - 1) * tile) / per;
+        for (int64_t k = kf; k <= kl; ++k) {
+          const int64_t t0 = k == kf ? 0 : (k * per - S + tile - 1) / tile;
+          const int64_t t1 = k == kl ? ntiles : ((k + 1) * per - S + tile - 1) / tile;
+          if (base < plan.max_items) {
+            plan.item[base] = make_int4(e / dcp, e % dcp, (int)(t0 * tile),
+                                        (int)(t1 * tile < len ? t1 * tile : len));
+            plan.ipart[base] = (int)k;
+          }
+          ++base;
+        }
+      }
+      S += len;
+    }
+  }
+  __syncthreads();
+  // pfirst[k] = first item whose run is >= k
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    const int k = plan.ipart[i], kp = i > 0 ? plan.ipart[i - 1] : -1;
+    for (int q = kp + 1; q <= k && q <= parts; ++q) plan.pfirst[q] = i;
+  }
+  if (threadIdx.x == 0) {
+    const int kl = total > 0 ? plan.ipart[total - 1] : -1;
+    for (int q = kl + 1; q <= parts; ++q) plan.pfirst[q] = total;
+    plan.off[n] = total;
+    plan.hdr[0] = total;
+    plan.hdr[1] = (int)(per < (1 << 30) ? per : (1 << 30));
+    plan.hdr[2] = 0;
+    plan.hdr[3] = 0;
+  }
+}
+
+int launch_plan_parts(const int32_t* local_lens, int B, int dcp, int tile, int parts,
+                      const Plan& plan, cudaStream_t s) {
+  if (parts < 1 || parts > kMaxParts || tile < 1) return DCP_EINVAL;
+  plan_parts_kernel<<<1, kPlanThreads, 0, s>>>(local_lens, B, dcp, tile, parts, plan);
   return launch_status();
 }
 

@@ -16,6 +16,8 @@ namespace dcp {
 
 int mla_target_items() { return 4 * num_sms(); }
 
+// The balanced-parts plan makes at most B*dcp + clusters - 1 items and the
+// chunked plan at most target + B*dcp; clusters <= SMs/2 < target.
 int mla_max_items(int B, int dcp) { return mla_target_items() + B * dcp; }
 
 }  // namespace dcp
@@ -38,10 +40,11 @@ int mla_split(const dcp_layout_t& layout, const void* q, int B, int Hq, int dk, 
               float scale, dcp_dtype_t dtype, const dcp_paged_kv_t& kv, const int32_t* local_lens,
               const Plan& plan, int32_t* err, cudaStream_t s) {
   if (mla_tc_supported(layout, B, Hq, dk, dv, dtype, kv)) {
-    int rc = launch_plan(local_lens, B, layout.dcp_size, 1, kMlaTcTile, kMlaTcMinChunk,
-                         mla_target_items(), plan, s);
+    const int clusters = mla_tc_clusters();
+    if (clusters < 1) return DCP_ECUDA;
+    int rc = launch_plan_parts(local_lens, B, layout.dcp_size, kMlaTcTile, clusters, plan, s);
     if (rc) return rc;
-    return launch_mla_tc(layout, q, B, Hq, scale, kv, plan, err, s);
+    return launch_mla_tc(layout, q, B, Hq, scale, kv, plan, clusters, err, s);
   }
   int rc = launch_plan(local_lens, B, layout.dcp_size, 1, 1, 64, mla_target_items(), plan, s);
   if (rc) return rc;

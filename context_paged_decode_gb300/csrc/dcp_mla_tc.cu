@@ -9,28 +9,32 @@
 //
 // Shape of the kernel:
 //  * one work item = a run of local positions of one request on one rank
-//    (the split-KV plan); items never cross a rank (each shard attends only
-//    its local KV, page "Decode Context Parallel (DCP)", section "Decode");
+//    (items never cross a rank: each shard attends only its local KV, page
+//    "Decode Context Parallel (DCP)", section "Decode").  Cluster k runs the
+//    contiguous items of run k of the balanced-parts plan, so every cluster
+//    gets the same number of tokens and consecutive items mostly share a
+//    request (its Q stays loaded);
 //  * a cluster of two CTAs per item.  The fp32 output tile 128 x 512 would
 //    fill all of tensor memory, so CTA c keeps value columns [256c, 256c+256).
 //    The 576-wide reduction of Q K^T is split the same way: CTA 0 reduces
 //    over latent columns 0..255, CTA 1 over 256..575 (latent 256..511 plus
-//    the 64 rope columns).  Each CTA therefore holds only its part of Q
-//    (64 or 80 KB) and of every KV stage (16 or 20 KB of a 32-token stage),
-//    which leaves room for five KV stages, and no MMA work is duplicated;
-//  * the two fp32 partial score tiles (128 x 32) are exchanged through
-//    distributed shared memory, one stage ahead of the softmax, and added
-//    (IEEE addition commutes, so both CTAs hold bit-identical scores and take
-//    identical softmax decisions);
-//  * warp 0 issues TMA (Q once per request, KV stages through a 5-deep
-//    ring), warp 1 issues tcgen05.mma (Q K^T runs three stages ahead of
-//    P V), warps 2-5 run the online softmax (one head row per thread; scores
-//    read from tensor memory, P written back to tensor memory as the A
-//    operand of P V) and the epilogue.  The softmax threads push their
-//    partial scores into the peer's shared memory with st.async, which
-//    completes transaction bytes on the peer's mbarrier without a fence on
-//    the sender; warp 6 arms this CTA's receive barrier for every stage and
-//    warp 7 tells the peer when a receive slot may be reused;
+//    the 64 rope columns), and the two fp32 partial score tiles are exchanged
+//    through distributed shared memory and added (IEEE addition commutes, so
+//    both CTAs hold bit-identical scores and take identical decisions);
+//  * a stage is 64 tokens: one tcgen05.mma instruction costs its issuing
+//    thread about as long as an N=64 product takes the tensor core, so Q K^T
+//    runs at N=64 (16 instructions per stage from tensor memory, plus 4 for
+//    the rope chunk, which CTA 1 keeps in shared memory);
+//  * tensor memory: O half (256 columns) | Q part (128) | two fp32 score
+//    buffers of 64 columns.  P (bf16, 128 x 64) goes to shared memory as the
+//    A operand of P V;
+//  * warp 0 issues TMA (a 3-deep ring of 64-token stages), warp 1 issues
+//    Q K^T (up to two stages ahead), warp 2 issues P V, warps 3-10 run the
+//    online softmax: the two warps of one tensor-memory lane quarter take 32
+//    of the 64 columns each and combine their row maxima through shared
+//    memory.  A softmax iteration first ships its 32 columns of the next
+//    stage's partial scores to the peer, then finishes the current stage
+//    with the peer's scores, which arrived one iteration ago;
 //  * the output is rescaled only when the running maximum grows by more
 //    than 8 (log2 units), so P stays <= 256 and the rare rescale waits for
 //    the in-flight P V.
@@ -39,16 +43,14 @@
 #include <stdlib.h>
 #include <string.h>
 
-#include <type_traits>
-
 #include "dcp_mla_tc.cuh"
 #include "dcp_ptx.cuh"
 
 namespace dcp {
 
 struct MlaTcArgs {
-  CUtensorMap qmap;                  // [B*128 rows][576] bf16, box 64 x 128
-  CUtensorMap kvmap[DCP_MAX_RANKS];  // [num_blocks*bs rows][576] bf16, box 64 x 32
+  CUtensorMap kvmap[DCP_MAX_RANKS];  // [num_blocks*bs rows][576] bf16, box 64 x 64
+  const uint16_t* q;                 // [B][128][576] bf16
   int B, bs, dcp;
   float sl2;
   const int32_t* bt;
@@ -61,46 +63,63 @@ struct MlaTcArgs {
 constexpr int kHeads = 128;
 constexpr int kDk = 576;
 constexpr int kDvHalf = 256;
-constexpr int kSt = 32;                              // tokens per KV stage
-constexpr int kNs = 5;                               // KV stages in flight
-constexpr int kMaxCh = 5;                            // 64-column chunks per CTA (CTA 1)
-constexpr int kQChunkBytes = kHeads * 128;           // 16 KB
-constexpr int kKvChunkBytes = kSt * 128;             // 4 KB
-constexpr int kKvStageBytes = kMaxCh * kKvChunkBytes;  // 20 KB
-constexpr int kXSlotBytes = kHeads * kSt * 4;        // 16 KB of fp32 partial scores
-constexpr int kKvOff = kMaxCh * kQChunkBytes;        // 80 KB
-constexpr int kXOff = kKvOff + kNs * kKvStageBytes;  // 180 KB
-constexpr int kBarOff = kXOff + 2 * kXSlotBytes;     // 212 KB
-constexpr int kNumBars = 32;
+constexpr int kSt = 64;                                // tokens per stage
+constexpr int kNs = 3;                                 // KV stages in flight
+constexpr int kMaxCh = 5;                              // 64-column chunks per CTA (CTA 1)
+constexpr int kChunkBytes = kSt * 128;                 // 8 KB: 64 tokens x 64 columns
+constexpr int kStageBytes = kMaxCh * kChunkBytes;      // 40 KB
+constexpr int kXSlotBytes = kHeads * kSt * 4;          // 32 KB of fp32 partial scores
+constexpr int kPBytes = kHeads * kSt * 2;              // 16 KB of bf16 P
+constexpr int kRopeBytes = kHeads * 128;               // 16 KB: Q rope chunk (CTA 1)
+constexpr int kKvOff = 0;
+constexpr int kXOff = kKvOff + kNs * kStageBytes;      // 120 KB
+constexpr int kPOff = kXOff + 2 * kXSlotBytes;         // 184 KB
+constexpr int kRopeOff = kPOff + kPBytes;              // 200 KB
+constexpr int kMaxOff = kRopeOff + kRopeBytes;         // 216 KB: half-row maxima [2][2][128]
+constexpr int kLsumOff = kMaxOff + 2 * 2 * kHeads * 4; // 218 KB: half-row sums [2][2][128]
+constexpr int kBarOff = kLsumOff + 2 * 2 * kHeads * 4; // 220 KB
+constexpr int kNumBars = 26;
 constexpr int kMlaSmem = 1024 + kBarOff + kNumBars * 8 + 16;
-constexpr int kMlaThreads = 256;
+constexpr int kSoftWarps = 8;
+constexpr int kFirstSoftWarp = 3;
+constexpr int kMlaThreads = 32 * (kFirstSoftWarp + kSoftWarps);  // 352
 constexpr uint32_t kTmemCols = 512;
-constexpr int kNsb = 4;                            // score buffers in tensor memory
-constexpr int kLookahead = 3;                      // Q K^T issued this many stages ahead of P V
-constexpr uint32_t kColO = 0, kColS = 256, kColP = 256 + kNsb * kSt;
+constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384;
 constexpr float kRescaleThreshold = 8.f;
 constexpr int kStuckMla = 1 << 20;
+
+static_assert(kColQ + 4 * 32 <= kColS && kColS + 2 * kSt <= kTmemCols, "tensor memory overflow");
+static_assert(kMlaSmem <= 227 * 1024, "shared memory overflow");
 
 // barrier slots
 enum : int {
   B_KV_FULL = 0,    // +stage (kNs)
-  B_KV_EMPTY = 5,   // +stage (kNs)
-  B_S_FULL = 10,    // +score buffer (kNsb)
-  B_S_FREE = 14,    // +score buffer (kNsb)
-  B_P_FULL = 18,    // +buffer
-  B_PV_DONE = 20,   // +buffer
-  B_X_FULL = 22,    // +slot: the peer's partial scores landed in my slot
-  B_X_FREE = 24,    // +slot: the peer consumed what I wrote into its slot
-  B_Q_FULL = 26,
-  B_Q_EMPTY = 27,
-  B_O_FULL = 28,
-  B_O_FREE = 29,
-  B_IB_DONE = 30   // +slot: my softmax threads finished reading the peer's scores
+  B_KV_EMPTY = 3,   // +stage (kNs)
+  B_S_FULL = 6,     // +score buffer
+  B_S_FREE = 8,     // +score buffer: every softmax warp has read it
+  B_P_FULL = 10,    // every softmax warp has stored its P columns
+  B_P_FREE = 11,    // the P V reading P has completed
+  B_X_FULL = 12,    // +slot: the peer's partial scores landed in my slot
+  B_X_FREE = 14,    // +slot: the peer's softmax warps consumed what I wrote into its slot
+  B_Q_FULL = 16,
+  B_Q_EMPTY = 17,
+  B_O_FULL = 18,
+  B_O_FREE = 19,
+  B_L_FULL = 20,    // +buffer: both halves' row sums of an item are in shared memory
+  B_L_FREE = 22,    // +buffer: both halves have read them
+  B_MX_FULL = 24    // +buffer: both halves' row maxima of a stage are in shared memory
 };
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kSt, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kDvHalf, false, true);
 
+__device__ __forceinline__ bool counted_by_warps(int i) {
+  return i == B_S_FREE || i == B_S_FREE + 1 || i == B_P_FULL || i == B_X_FREE ||
+         i == B_X_FREE + 1 || i == B_Q_FULL || i == B_O_FREE || i >= B_L_FULL;
+}
+
+// Eleven warps put three on some SM sub-partitions (16K registers each), so a
+// thread may hold at most 168 registers.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
 mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
   extern __shared__ uint8_t smem_raw[];
@@ -111,22 +130,18 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();          // 0 or 1: which half this CTA owns
   const uint32_t peer = crank ^ 1u;
-  const int nch = crank == 0 ? 4 : 5;                // K^T chunks reduced here
-  const int ch0 = crank == 0 ? 0 : 4;                // first global 64-column chunk
-  const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
-  const int n_items = plan.hdr[0];
+  const int nch = crank == 0 ? 4 : 5;                // 64-column chunks reduced here
+  const int ch0 = crank == 0 ? 0 : 4;                // first global chunk
+  const int cl = blockIdx.x >> 1;
+  const int i0 = plan.pfirst[cl], i1 = plan.pfirst[cl + 1];
   int32_t* errp = A.err ? A.err : plan.hdr + 3;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) {
-      uint32_t cnt = 1;
-      if ((i >= B_S_FREE && i < B_S_FREE + kNsb) || i == B_P_FULL || i == B_P_FULL + 1 ||
-          i == B_O_FREE || i >= B_IB_DONE)
-        cnt = 128;                                  // every softmax thread arrives
-      mbar_init(bars + 8 * i, cnt);
-    }
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bars + 8 * i, counted_by_warps(i) ? kSoftWarps : 1);
+    // the receive slots of stages 0 and 1 expect the peer's 32 KB each
+    mbar_arrive_expect_tx(bars + 8 * B_X_FULL, kXSlotBytes);
+    mbar_arrive_expect_tx(bars + 8 * (B_X_FULL + 1), kXSlotBytes);
     fence_mbar_init();
-    prefetch_tmap(&A.qmap);
     for (int r = 0; r < A.dcp; ++r) prefetch_tmap(&A.kvmap[r]);
   }
   if (warp == 1) {
@@ -134,7 +149,7 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
     tc_relinquish();
   }
   tc_fence_before();
-  cluster_sync();  // barriers of both CTAs initialised before any remote arrive
+  cluster_sync();  // barriers of both CTAs initialised before any remote access
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -144,178 +159,148 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
     return vb < A.max_vb ? (int64_t)__ldg(A.bt + r * A.bt_rank_stride + (int64_t)b * A.max_vb + vb)
                          : (int64_t)-1;
   };
-  // physical row of stage j of an item, false if the block-table entry is unusable
-  auto stage_row = [&](int b, int r, int p0, int j, int& row) -> bool {
-    const int p = p0 + j * kSt;
-    const int vb = p / A.bs, off = p - vb * A.bs;
-    const int64_t phys =
-        vb < A.max_vb ? (int64_t)__ldg(A.bt + r * A.bt_rank_stride + (int64_t)b * A.max_vb + vb)
-                      : (int64_t)-1;
-    if (phys < 0 || phys >= A.num_blocks) return false;
-    row = (int)(phys * A.bs + off);
-    return true;
-  };
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ---------------- TMA producer ----------------
-    uint32_t g = 0, k = 0;
-    int prev_b = -1;
-    bool dead = false;
-    for (int it = cl; it < n_items && !dead; it += ncl, ++k) {
-      const int4 d = plan.item[it];
-      const int b = d.x, r = d.y & 255, p0 = d.z, p1 = d.w;
-      const int nst = (p1 - p0 + kSt - 1) / kSt;
-      if (!mbar_wait(bars + 8 * B_Q_EMPTY, (k & 1) ^ 1)) {
-        dead = true;
-        break;
-      }
-      if (b != prev_b) {
-        mbar_arrive_expect_tx(bars + 8 * B_Q_FULL, nch * kQChunkBytes);
-        for (int c = 0; c < nch; ++c)
-          tma_load_2d(sbase + c * kQChunkBytes, &A.qmap, 64 * (ch0 + c), b * kHeads,
-                      bars + 8 * B_Q_FULL);
-        prev_b = b;
-      } else {
-        mbar_arrive(bars + 8 * B_Q_FULL);
-      }
-      for (int j = 0; j < nst; ++j, ++g) {
-        const uint32_t st = g % kNs, u = g / kNs;
-        if (!mbar_wait(bars + 8 * (B_KV_EMPTY + st), (u & 1) ^ 1)) {
-          dead = true;
-          break;
-        }
-        const uint32_t full = bars + 8 * (B_KV_FULL + st);
-        int row;
-        if (stage_row(b, r, p0, j, row)) {
-          mbar_arrive_expect_tx(full, nch * kKvChunkBytes);
-          const uint32_t dst = sbase + kKvOff + st * kKvStageBytes;
-          for (int c = 0; c < nch; ++c)
-            tma_load_2d(dst + c * kKvChunkBytes, &A.kvmap[r], 64 * (ch0 + c), row, full);
-        } else {
-          if (crank == 0) count_error(A.err);
-          mbar_arrive(full);
-        }
-      }
-    }
-    if (dead) atomicAdd(errp, kStuckMla);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- tcgen05.mma issuer ----------------
-    uint32_t g = 0, k = 0;
-    bool dead = false;
-    const uint32_t d_o = tmem + kColO;
-    auto qk_issue = [&](auto nch_c, uint32_t d_s, uint32_t kv) {
-      constexpr int NCH = decltype(nch_c)::value;
-      const uint64_t a0 = sdesc_sw128(sbase, 0, 1024);
-      const uint64_t b0 = sdesc_sw128(kv, 0, 1024);
-#pragma unroll
-      for (int c = 0; c < NCH; ++c)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc_mma_ss(d_s, a0 + (uint64_t)((c * kQChunkBytes + kk * 32) >> 4),
-                    b0 + (uint64_t)((c * kKvChunkBytes + kk * 32) >> 4), kIdescQK, (c | kk) != 0);
-    };
-    auto qk = [&](uint32_t gs) -> bool {
-      const uint32_t st = gs % kNs, u = gs / kNs, sb = gs % kNsb, us = gs / kNsb;
-      if (!mbar_wait(bars + 8 * (B_KV_FULL + st), u & 1)) return false;
-      if (!mbar_wait(bars + 8 * (B_S_FREE + sb), (us & 1) ^ 1)) return false;
-      tc_fence_after();
-      const uint32_t d_s = tmem + kColS + sb * kSt;
-      const uint32_t kv = sbase + kKvOff + st * kKvStageBytes;
-      if (nch == 4)
-        qk_issue(std::integral_constant<int, 4>{}, d_s, kv);
-      else
-        qk_issue(std::integral_constant<int, 5>{}, d_s, kv);
-      tc_commit(bars + 8 * (B_S_FULL + sb));
-      return true;
-    };
-    auto pv = [&](uint32_t gs, bool first) -> bool {
-      const uint32_t st = gs % kNs, pb = gs & 1, up = gs >> 1;
-      if (!mbar_wait(bars + 8 * (B_P_FULL + pb), up & 1)) return false;
-      if (first && !mbar_wait(bars + 8 * B_O_FREE, (k & 1) ^ 1)) return false;
-      tc_fence_after();
-      // V = this CTA's four value chunks, the MN-major B operand: 64-column
-      // atoms kKvChunkBytes apart, 8-token groups 1024 B apart; the second
-      // k-step starts 16 tokens in.
-      const uint32_t v = sbase + kKvOff + st * kKvStageBytes;
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const uint64_t bd = sdesc_sw128(v + kk * 16 * 128, kKvChunkBytes, 1024);
-        tc_mma_ts(d_o, tmem + kColP + pb * 16 + kk * 8, bd, kIdescPV, (!first || kk) ? 1u : 0u);
-      }
-      tc_commit(bars + 8 * (B_KV_EMPTY + st));
-      tc_commit(bars + 8 * (B_PV_DONE + pb));
-      return true;
-    };
-    for (int it = cl; it < n_items && !dead; it += ncl, ++k) {
-      const int4 d = plan.item[it];
-      const int nst = (d.w - d.z + kSt - 1) / kSt;
-      if (!mbar_wait(bars + 8 * B_Q_FULL, k & 1)) {
-        dead = true;
-        break;
-      }
-      tc_fence_after();
-      for (int j = 0; j < kLookahead && j < nst; ++j)
-        if (!qk(g + j)) {
-          dead = true;
-          break;
-        }
-      for (int j = 0; j < nst && !dead; ++j) {
-        if (!pv(g + j, j == 0)) {
-          dead = true;
-          break;
-        }
-        if (j + kLookahead < nst && !qk(g + j + kLookahead)) {
-          dead = true;
-          break;
-        }
-      }
-      if (dead) break;
-      g += nst;
-      tc_commit(bars + 8 * B_O_FULL);
-      tc_commit(bars + 8 * B_Q_EMPTY);
-    }
-    if (dead) atomicAdd(errp, kStuckMla);
-  } else if (warp >= 6) {
-    // ---------------- exchange helpers ----------------
-    // warp 6: arm X_FULL of each stage with the 16 KB the peer will st.async
-    //         into this CTA (after the slot's previous phase completed)
-    // warp 7: I consumed the peer's scores -> arrive on the peer's X_FREE
     if (lane == 0) {
-      const uint32_t free_remote = mapa_shared(bars + 8 * B_X_FREE, peer);
+      const uint64_t pol = policy_evict_first();
       uint32_t g = 0;
       bool dead = false;
-      for (int it = cl; it < n_items && !dead; it += ncl) {
+      for (int it = i0; it < i1 && !dead; ++it) {
         const int4 d = plan.item[it];
-        const int nst = (d.w - d.z + kSt - 1) / kSt;
+        const int b = d.x, r = d.y & 255, p0 = d.z, p1 = d.w;
+        const int nst = (p1 - p0 + kSt - 1) / kSt;
         for (int j = 0; j < nst; ++j, ++g) {
-          const uint32_t xs = g & 1, ux = g >> 1;
-          if (warp == 6) {
-            if (ux > 0 && !mbar_wait(bars + 8 * (B_X_FULL + xs), (ux - 1) & 1)) {
-              dead = true;
-              break;
-            }
-            mbar_arrive_expect_tx(bars + 8 * (B_X_FULL + xs), kXSlotBytes);
+          const uint32_t st = g % kNs, u = g / kNs;
+          const int64_t phys = bt_phys(b, r, p0, j);
+          if (!mbar_wait(bars + 8 * (B_KV_EMPTY + st), (u & 1) ^ 1)) {
+            dead = true;
+            break;
+          }
+          const uint32_t full = bars + 8 * (B_KV_FULL + st);
+          const int p = p0 + j * kSt;
+          const int off = p - (p / A.bs) * A.bs;
+          if (phys >= 0 && phys < A.num_blocks) {
+            const int row = (int)(phys * A.bs + off);
+            mbar_arrive_expect_tx(full, nch * kChunkBytes);
+            const uint32_t dst = sbase + kKvOff + st * kStageBytes;
+            for (int c = 0; c < nch; ++c)
+              tma_load_2d_hint(dst + c * kChunkBytes, &A.kvmap[r], 64 * (ch0 + c), row, full, pol);
           } else {
-            if (!mbar_wait(bars + 8 * (B_IB_DONE + xs), ux & 1)) {
-              dead = true;
-              break;
-            }
-            mbar_arrive_remote(free_remote + 8 * xs);
+            if (crank == 0) count_error(A.err);
+            mbar_arrive(full);
           }
         }
       }
       if (dead) atomicAdd(errp, kStuckMla);
     }
-  } else if (warp >= 2) {
-    // ---------------- softmax + epilogue (one head row per thread) ----------------
+  } else if (warp == 1) {
+    // ---------------- Q K^T issuer ----------------
+    if (lane == 0) {
+      uint32_t g = 0, qv = 0;
+      int prev_b = -1;
+      bool dead = false;
+      const uint64_t rope_a = sdesc_sw128(sbase + kRopeOff, 0, 1024);
+      for (int it = i0; it < i1 && !dead; ++it) {
+        const int4 d = plan.item[it];
+        const int b = d.x;
+        const int nst = (d.w - d.z + kSt - 1) / kSt;
+        const bool q_last = it + 1 >= i1 || plan.item[it + 1].x != b;
+        if (b != prev_b) {
+          if (!mbar_wait(bars + 8 * B_Q_FULL, qv & 1)) {
+            dead = true;
+            break;
+          }
+          ++qv;
+          prev_b = b;
+        }
+        for (int j = 0; j < nst; ++j) {
+          const uint32_t gs = g + j;
+          const uint32_t st = gs % kNs, u = gs / kNs, sb = gs & 1, us = gs >> 1;
+          if (!mbar_wait(bars + 8 * (B_KV_FULL + st), u & 1) ||
+              !mbar_wait(bars + 8 * (B_S_FREE + sb), (us & 1) ^ 1)) {
+            dead = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_s = tmem + kColS + sb * kSt;
+          const uint64_t b0 = sdesc_sw128(sbase + kKvOff + st * kStageBytes, 0, 1024);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_ts(d_s, tmem + kColQ + c * 32 + kk * 8,
+                        b0 + (uint64_t)((c * kChunkBytes + kk * 32) >> 4), kIdescQK,
+                        (c | kk) != 0);
+          if (nch == 5) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_ss(d_s, rope_a + (uint64_t)((kk * 32) >> 4),
+                        b0 + (uint64_t)((4 * kChunkBytes + kk * 32) >> 4), kIdescQK, 1u);
+          }
+          tc_commit(bars + 8 * (B_S_FULL + sb));
+          if (q_last && j == nst - 1) tc_commit(bars + 8 * B_Q_EMPTY);  // last reader of this Q
+        }
+        if (dead) break;
+        if (nst == 0 && q_last) tc_commit(bars + 8 * B_Q_EMPTY);
+        g += nst;
+      }
+      if (dead) atomicAdd(errp, kStuckMla);
+    }
+  } else if (warp == 2) {
+    // ---------------- P V issuer ----------------
+    if (lane == 0) {
+      uint32_t g = 0, k = 0;
+      bool dead = false;
+      const uint64_t p_a = sdesc_sw128(sbase + kPOff, 0, 1024);
+      for (int it = i0; it < i1 && !dead; ++it, ++k) {
+        const int4 d = plan.item[it];
+        const int nst = (d.w - d.z + kSt - 1) / kSt;
+        for (int j = 0; j < nst; ++j) {
+          const uint32_t gs = g + j, st = gs % kNs;
+          if (!mbar_wait(bars + 8 * B_P_FULL, gs & 1) ||
+              (j == 0 && !mbar_wait(bars + 8 * B_O_FREE, (k & 1) ^ 1))) {
+            dead = true;
+            break;
+          }
+          tc_fence_after();
+          // V = this CTA's four value chunks, the MN-major B operand: 64-column
+          // atoms kChunkBytes apart, 8-token groups 1024 B apart; k-step kk
+          // starts 16 tokens further.  P is the K-major A operand.
+          const uint32_t v = sbase + kKvOff + st * kStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = sdesc_sw128(v + kk * 16 * 128, kChunkBytes, 1024);
+            tc_mma_ss(tmem + kColO, p_a + (uint64_t)((kk * 32) >> 4), bd, kIdescPV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(bars + 8 * (B_KV_EMPTY + st));
+          tc_commit(bars + 8 * B_P_FREE);
+        }
+        if (dead) break;
+        g += nst;
+        tc_commit(bars + 8 * B_O_FULL);
+      }
+      if (dead) atomicAdd(errp, kStuckMla);
+    }
+  } else {
+    // ---------------- softmax + epilogue ----------------
+    const int sw = warp - kFirstSoftWarp;    // 0..7
+    const int hf = sw >> 2;                  // which 32 of the 64 stage columns
     const int q4 = warp & 3;                 // tensor-memory lane quarter of this warp
     const int head = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const int tid = threadIdx.x - 64;        // 0..127
-    const uint32_t xrow = sbase + kXOff + head * 128;      // my row of my exchange slots
+    const int stid = sw * 32 + lane;         // 0..255
+    const bool armer = sw == 0 && lane == 0;
+    const uint32_t xrow = sbase + kXOff + head * 256;      // my row of my receive slots
     const uint32_t xrow_peer = mapa_shared(xrow, peer);    // my row of the peer's slots
     const uint32_t xfull_peer = mapa_shared(bars + 8 * B_X_FULL, peer);
-    uint32_t g = 0, k = 0;
+    const uint32_t xfree_peer = mapa_shared(bars + 8 * B_X_FREE, peer);
+    const uint32_t prow = sbase + kPOff + head * 128;
+    float* hmax = reinterpret_cast<float*>(smem + kMaxOff);  // [2][2][128]
+    float* lsum = reinterpret_cast<float*>(smem + kLsumOff);  // [2][2][128]
+    uint32_t g = 0, k = 0, qv = 0;
+    int prev_b = -1;
     bool dead = false;
     // tcgen05.ld/st are warp-collective: every wait outcome is made warp-uniform
     auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
@@ -324,142 +309,238 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
     auto wwait_cl = [&](uint32_t bar, uint32_t par) -> bool {
       return __all_sync(0xffffffffu, mbar_wait_cluster(bar, par));
     };
-    // read this CTA's partial scores of stage gs and ship them to the peer
-    auto send = [&](uint32_t gs, uint32_t (&mine)[32]) -> bool {
-      const uint32_t sb = gs % kNsb, us = gs / kNsb, xs = gs & 1, ux = gs >> 1;
+    auto warp_arrive = [&](uint32_t bar) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+    };
+    // ship my 32 columns of this CTA's partial scores of stage gs to the peer
+    auto ship = [&](uint32_t gs) -> bool {
+      const uint32_t sb = gs & 1, us = gs >> 1;
       if (!wwait(bars + 8 * (B_S_FULL + sb), us & 1)) return false;
       tc_fence_after();
-      tc_ld32(tmem + lane_off + kColS + sb * kSt, mine);
+      uint32_t mine[32];
+      tc_ld32(tmem + lane_off + kColS + sb * kSt + hf * 32, mine);
       tc_wait_ld(mine);
-      tc_fence_before();
-      mbar_arrive(bars + 8 * (B_S_FREE + sb));
-      // the peer must have consumed what I put in its slot two stages ago
-      if (!wwait_cl(bars + 8 * (B_X_FREE + xs), (ux & 1) ^ 1)) return false;
-      const uint32_t dst = xrow_peer + xs * kXSlotBytes;
-      const uint32_t bar = xfull_peer + 8 * xs;
+      // the peer must have consumed what I put in this slot two stages ago
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait_relaxed_cluster(bars + 8 * (B_X_FREE + sb), (us & 1) ^ 1)))
+        return false;
+      const uint32_t dst = xrow_peer + sb * kXSlotBytes;
+      const uint32_t bar = xfull_peer + 8 * sb;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        st_async_v4(dst + ((i ^ (head & 7)) << 4), mine[4 * i], mine[4 * i + 1], mine[4 * i + 2],
-                    mine[4 * i + 3], bar);
+      for (int t = 0; t < 8; ++t) {
+        const int i = hf * 8 + t;  // 16-byte unit of the 256-byte row
+        st_async_v4(dst + ((i ^ (head & 15)) << 4), mine[4 * t], mine[4 * t + 1], mine[4 * t + 2],
+                    mine[4 * t + 3], bar);
+      }
       return true;
     };
-    // add the peer's partial scores of stage gs to mine
-    auto recv = [&](uint32_t gs, const uint32_t (&mine)[32], float (&sc)[32]) -> bool {
-      const uint32_t xs = gs & 1, ux = gs >> 1;
-      if (!wwait_cl(bars + 8 * (B_X_FULL + xs), ux & 1)) return false;
-      const uint32_t src = xrow + xs * kXSlotBytes;
+    // my 32 columns of the full scores of stage gs: this CTA's partial (read
+    // again from tensor memory, then the buffer is released) plus the peer's
+    auto gather = [&](uint32_t gs, float (&sc)[32]) -> bool {
+      const uint32_t sb = gs & 1, us = gs >> 1;
+      if (!wwait_cl(bars + 8 * (B_X_FULL + sb), us & 1)) return false;
+      uint32_t mine[32];
+      tc_ld32(tmem + lane_off + kColS + sb * kSt + hf * 32, mine);
+      tc_wait_ld(mine);
+      tc_fence_before();
+      warp_arrive(bars + 8 * (B_S_FREE + sb));
+      const uint32_t src = xrow + sb * kXSlotBytes;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int t = 0; t < 8; ++t) {
+        const int i = hf * 8 + t;
         uint32_t a, bq, c, d;
         asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(a), "=r"(bq), "=r"(c), "=r"(d)
-                     : "r"(src + ((i ^ (head & 7)) << 4)));
-        sc[4 * i + 0] = __uint_as_float(mine[4 * i + 0]) + __uint_as_float(a);
-        sc[4 * i + 1] = __uint_as_float(mine[4 * i + 1]) + __uint_as_float(bq);
-        sc[4 * i + 2] = __uint_as_float(mine[4 * i + 2]) + __uint_as_float(c);
-        sc[4 * i + 3] = __uint_as_float(mine[4 * i + 3]) + __uint_as_float(d);
+                     : "r"(src + ((i ^ (head & 15)) << 4)));
+        sc[4 * t + 0] = __uint_as_float(mine[4 * t + 0]) + __uint_as_float(a);
+        sc[4 * t + 1] = __uint_as_float(mine[4 * t + 1]) + __uint_as_float(bq);
+        sc[4 * t + 2] = __uint_as_float(mine[4 * t + 2]) + __uint_as_float(c);
+        sc[4 * t + 3] = __uint_as_float(mine[4 * t + 3]) + __uint_as_float(d);
       }
-      mbar_arrive(bars + 8 * (B_IB_DONE + xs));  // warp 7 frees the slot on the peer
+      // the slot's next phase (stage gs + 2) expects the peer's 32 KB again
+      if (armer) mbar_arrive_expect_tx(bars + 8 * (B_X_FULL + sb), kXSlotBytes);
+      // every loaded value feeds `dep`, so the loads complete before the arrival
+      float dep = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) dep += sc[i];
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer + 8 * sb, dep);
       return true;
     };
-    for (int it = cl; it < n_items && !dead; it += ncl, ++k) {
+    for (int it = i0; it < i1 && !dead; ++it, ++k) {
       const int4 d = plan.item[it];
       const int b = d.x, r = d.y & 255, p0 = d.z, p1 = d.w;
       const int nst = (p1 - p0 + kSt - 1) / kSt;
-      float m = -INFINITY, l = 0.f;
-      // block-table entries of the current and next stage, loaded ahead of use
-      int64_t ph_cur = bt_phys(b, r, p0, 0);
-      int64_t ph_next = nst > 1 ? bt_phys(b, r, p0, 1) : 0;
-      uint32_t cur[32];
-      if (!send(g, cur)) {
-        dead = true;
-        break;
-      }
-      for (int j = 0; j < nst; ++j) {
-        const uint32_t gj = g + j, pb = gj & 1, up = gj >> 1;
-        uint32_t nxt[32];
-        if (j + 1 < nst && !send(gj + 1, nxt)) {
-          dead = true;
-          break;
-        }
-        float sc[32];
-        if (!recv(gj, cur, sc)) {
-          dead = true;
-          break;
-        }
-        const int nvalid = (ph_cur >= 0 && ph_cur < A.num_blocks) ? min(kSt, p1 - (p0 + j * kSt)) : 0;
-        ph_cur = ph_next;
-        if (j + 2 < nst) ph_next = bt_phys(b, r, p0, j + 2);  // consumed two stages later
-        float x[32];
-        float mx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          x[i] = i < nvalid ? sc[i] * A.sl2 : -INFINITY;
-          mx = fmaxf(mx, x[i]);
-        }
-        const bool grow = mx > m + kRescaleThreshold;
-        const bool need = grow && j > 0 && l > 0.f;  // O already holds this row's sums
-        if (__any_sync(0xffffffffu, need)) {
-          // wait for the in-flight P V, then rescale the rows that need it
-          const uint32_t gp = gj - 1;
-          if (!wwait(bars + 8 * (B_PV_DONE + (gp & 1)), (gp >> 1) & 1)) {
-            dead = true;
-            break;
-          }
-          tc_fence_after();
-          const float f = need ? exp2f(m - mx) : 1.f;
-#pragma unroll 1
-          for (int cc = 0; cc < kDvHalf / 32; ++cc) {
-            uint32_t o[32];
-            tc_ld32(tmem + lane_off + kColO + cc * 32, o);
-            tc_wait_ld(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-            tc_st32(tmem + lane_off + kColO + cc * 32, o);
-          }
-          tc_wait_st();
-          l *= f;
-        }
-        if (grow) m = mx;
-        const float mb = (m == -INFINITY) ? 0.f : m;
-        uint32_t pk[16];
-        float ls = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float pa = ex2_ftz(x[2 * i] - mb), pq = ex2_ftz(x[2 * i + 1] - mb);
-          ls += pa + pq;
-          pk[i] = pack_bf16(pa, pq);
-        }
-        l += ls;
-        // P buffer pb is free once the P V of two stages ago completed
-        if (!wwait(bars + 8 * (B_PV_DONE + pb), (up & 1) ^ 1)) {
+      if (b != prev_b) {
+        // load this half's share of Q row `head`: two 64-column chunks into
+        // tensor memory and (CTA 1) half of the rope chunk into shared memory,
+        // once the previous Q's last Q K^T has completed
+        if (qv > 0 && !wwait(bars + 8 * B_Q_EMPTY, (qv - 1) & 1)) {
           dead = true;
           break;
         }
         tc_fence_after();
-        tc_st16(tmem + lane_off + kColP + pb * 16, pk);
-        tc_wait_st();
-        if (nvalid < kSt) {
-          // rows past the end may hold anything: zero this CTA's V columns so 0 * x stays 0
-          const uint32_t v = sbase + kKvOff + (gj % kNs) * kKvStageBytes;
-          const int total = (kSt - nvalid) * 4 * 8;
-          for (int i = tid; i < total; i += 128) {
-            const int rr = nvalid + (i >> 5), ch = (i >> 3) & 3, part = i & 7;
-            asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
-                             v + ch * kKvChunkBytes + rr * 128 + part * 16),
-                         "r"(0u)
+        const uint4* src = reinterpret_cast<const uint4*>(
+            A.q + ((int64_t)b * kHeads + head) * kDk + (int64_t)ch0 * 64);
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int c = 2 * hf + c2;
+          uint32_t v[32];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const uint4 x = __ldg(src + c * 8 + t);
+            v[4 * t] = x.x;
+            v[4 * t + 1] = x.y;
+            v[4 * t + 2] = x.z;
+            v[4 * t + 3] = x.w;
+          }
+          tc_st32(tmem + lane_off + kColQ + c * 32, v);
+        }
+        if (nch == 5) {
+          const uint32_t rrow = sbase + kRopeOff + head * 128;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int u = hf * 4 + t;
+            const uint4 x = __ldg(src + 4 * 8 + u);
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rrow + ((u ^ (head & 7)) << 4)),
+                         "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w)
                          : "memory");
           }
           fence_proxy_async_smem();
         }
+        tc_wait_st();
         tc_fence_before();
-        mbar_arrive(bars + 8 * (B_P_FULL + pb));
+        warp_arrive(bars + 8 * B_Q_FULL);
+        ++qv;
+        prev_b = b;
+      }
+      float m = -INFINITY, lh = 0.f;
+      // block-table entries, loaded three stages ahead of use
+      int64_t ph[4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
+      for (int i = 0; i < 4; ++i) ph[i] = i < nst ? bt_phys(b, r, p0, i) : 0;
+      if (nst > 0 && !ship(g)) {
+        dead = true;
+        break;
+      }
+      for (int j = 0; j < nst; ++j) {
+        const uint32_t gj = g + j, mb_buf = gj & 1;
+        if (j + 1 < nst && !ship(gj + 1)) {
+          dead = true;
+          break;
+        }
+        float sc[32];
+        if (!gather(gj, sc)) {
+          dead = true;
+          break;
+        }
+        const int64_t phj = ph[0];
+        ph[0] = ph[1];
+        ph[1] = ph[2];
+        ph[2] = ph[3];
+        if (j + 4 < nst) ph[3] = bt_phys(b, r, p0, j + 4);
+        const int nvalid = (phj >= 0 && phj < A.num_blocks) ? min(kSt, p1 - (p0 + j * kSt)) : 0;
+        const int nv = nvalid - hf * 32;     // valid columns among mine
+        // row maximum of my 32 columns (raw scores; the scale is positive)
+        float t16[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = 2 * i < nv ? sc[2 * i] : -INFINITY;
+          const float c = 2 * i + 1 < nv ? sc[2 * i + 1] : -INFINITY;
+          t16[i] = fmaxf(a, c);
+        }
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) t16[i] = fmaxf(t16[i], t16[i + w]);
+        hmax[(mb_buf * 2 + hf) * kHeads + head] = t16[0] * A.sl2;
+        warp_arrive(bars + 8 * (B_MX_FULL + mb_buf));
+        if (!wwait(bars + 8 * (B_MX_FULL + mb_buf), (gj >> 1) & 1)) {
+          dead = true;
+          break;
+        }
+        const float mx = fmaxf(hmax[(mb_buf * 2) * kHeads + head],
+                               hmax[(mb_buf * 2 + 1) * kHeads + head]);
+        // P (single buffer) and O are free once the P V of the previous stage completed
+        if (!wwait(bars + 8 * B_P_FREE, (gj & 1) ^ 1)) {
+          dead = true;
+          break;
+        }
+        const bool grow = mx > m + kRescaleThreshold;
+        const bool need = grow && j > 0 && m > -INFINITY;  // O already holds this row's sums
+        if (__any_sync(0xffffffffu, need)) {
+          tc_fence_after();
+          const float f = need ? exp2f(m - mx) : 1.f;
+#pragma unroll 1
+          for (int cc = 0; cc < kDvHalf / 64; ++cc) {
+            uint32_t o[32];
+            const uint32_t ta = tmem + lane_off + kColO + hf * (kDvHalf / 2) + cc * 32;
+            tc_ld32(ta, o);
+            tc_wait_ld(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+            tc_st32(ta, o);
+          }
+          tc_wait_st();
+          lh *= f;
+        }
+        if (grow) m = mx;
+        const float mb = (m == -INFINITY) ? 0.f : m;
+        float ls = 0.f;
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float pa = 2 * i < nv ? ex2_ftz(fmaf(sc[2 * i], A.sl2, -mb)) : 0.f;
+          const float pq = 2 * i + 1 < nv ? ex2_ftz(fmaf(sc[2 * i + 1], A.sl2, -mb)) : 0.f;
+          ls += pa + pq;
+          pk[i] = pack_bf16(pa, pq);
+        }
+        lh += ls;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int u = hf * 4 + t;
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((u ^ (head & 7)) << 4)),
+                       "r"(pk[4 * t]), "r"(pk[4 * t + 1]), "r"(pk[4 * t + 2]), "r"(pk[4 * t + 3])
+                       : "memory");
+        }
+        if (nvalid < kSt) {
+          // rows past the end may hold anything: zero this CTA's V columns so 0 * x stays 0
+          const uint32_t st = gj % kNs;
+          if (!wwait(bars + 8 * (B_KV_FULL + st), (gj / kNs) & 1)) {
+            dead = true;
+            break;
+          }
+          const uint32_t v = sbase + kKvOff + st * kStageBytes;
+          const int total = (kSt - nvalid) * 4 * 8;
+          for (int i = stid; i < total; i += 32 * kSoftWarps) {
+            const int rr = nvalid + (i >> 5), ch = (i >> 3) & 3, part = i & 7;
+            asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
+                             v + ch * kChunkBytes + rr * 128 + part * 16),
+                         "r"(0u)
+                         : "memory");
+          }
+        }
+        fence_proxy_async_smem();   // P and zeroed V rows are read by the tensor core
+        warp_arrive(bars + 8 * B_P_FULL);
       }
       if (dead) break;
       g += nst;
-      // epilogue: O / l -> item partial, LSE in natural log
+      // epilogue: O / l -> item partial, LSE in natural log.  The row sum is
+      // the sum of the two halves' sums, exchanged through shared memory.
+      const uint32_t lb = k & 1, ul = k >> 1;
+      if (!wwait(bars + 8 * (B_L_FREE + lb), (ul & 1) ^ 1)) {
+        dead = true;
+        break;
+      }
+      lsum[(lb * 2 + hf) * kHeads + head] = lh;
+      warp_arrive(bars + 8 * (B_L_FULL + lb));
+      if (!wwait(bars + 8 * (B_L_FULL + lb), ul & 1)) {
+        dead = true;
+        break;
+      }
+      const float l = lsum[(lb * 2) * kHeads + head] + lsum[(lb * 2 + 1) * kHeads + head];
+      warp_arrive(bars + 8 * (B_L_FREE + lb));
       if (!wwait(bars + 8 * B_O_FULL, k & 1)) {
         dead = true;
         break;
@@ -467,22 +548,26 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
       tc_fence_after();
       const bool any = l > 0.f;
       const float inv = any ? 1.f / l : 0.f;
-      float* dst = plan.o + ((int64_t)it * kHeads + head) * (2 * kDvHalf) + crank * kDvHalf;
+      float* dst = plan.o + ((int64_t)it * kHeads + head) * (2 * kDvHalf) + crank * kDvHalf +
+                   hf * (kDvHalf / 2);
 #pragma unroll 1
-      for (int cc = 0; cc < kDvHalf / 32; ++cc) {
+      for (int cc = 0; cc < kDvHalf / 64; ++cc) {
         uint32_t o[32];
-        tc_ld32(tmem + lane_off + kColO + cc * 32, o);
+        tc_ld32(tmem + lane_off + kColO + hf * (kDvHalf / 2) + cc * 32, o);
         tc_wait_ld(o);
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(dst + cc * 32 + i) =
-              make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
-                          __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+        for (int i = 0; i < 32; i += 4) {
+          float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (any)
+            w = make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
+                            __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+          *reinterpret_cast<float4*>(dst + cc * 32 + i) = w;
+        }
       }
-      if (crank == 0)
+      if (crank == 0 && hf == 0)
         plan.lse[(int64_t)it * kHeads + head] = any ? (m + log2f(l)) * kLn2 : -INFINITY;
       tc_fence_before();
-      mbar_arrive(bars + 8 * B_O_FREE);
+      warp_arrive(bars + 8 * B_O_FREE);
     }
     if (dead && lane == 0) atomicAdd(errp, kStuckMla);
   }
@@ -497,6 +582,13 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
   cluster_sync();  // no CTA leaves while its peer may still touch its shared memory
 }
 
+namespace {
+
+int g_clusters[64] = {0};
+bool g_attr_done[64] = {false};
+
+}  // namespace
+
 bool mla_tc_supported(const dcp_layout_t& layout, int B, int Hq, int dk, int dv,
                       dcp_dtype_t dtype, const dcp_paged_kv_t& kv) {
   if (dtype != DCP_BF16 || Hq != kHeads || dk != kDk || dv != 2 * kDvHalf) return false;
@@ -509,39 +601,20 @@ bool mla_tc_supported(const dcp_layout_t& layout, int B, int Hq, int dk, int dv,
   return tensor_map_encoder() != nullptr;
 }
 
-int launch_mla_tc(const dcp_layout_t& layout, const void* q, int B, int Hq, float scale,
-                  const dcp_paged_kv_t& kv, const Plan& plan, int32_t* err, cudaStream_t s) {
-  (void)Hq;
-  if ((uintptr_t)q & 15) return DCP_EUNSUPPORTED;
-  MlaTcArgs A;
-  memset(&A, 0, sizeof(A));
-  if (!encode_2d_bf16_sw128(&A.qmap, q, kDk, (uint64_t)B * kHeads, kDk * 2, 64, kHeads))
-    return DCP_ECUDA;
-  const uint64_t rows = (uint64_t)kv.num_blocks * layout.block_size;
-  for (int r = 0; r < layout.dcp_size; ++r)
-    if (!encode_2d_bf16_sw128(&A.kvmap[r], kv.k.ptr[r], kDk, rows > 0 ? rows : 1, kDk * 2, 64,
-                              kSt))
-      return DCP_ECUDA;
-  A.B = B;
-  A.bs = layout.block_size;
-  A.dcp = layout.dcp_size;
-  A.sl2 = scale * kLog2e;
-  A.bt = kv.block_table;
-  A.max_vb = kv.max_vblocks;
-  A.bt_rank_stride = kv.bt_rank_stride;
-  A.num_blocks = kv.num_blocks;
-  A.err = err;
-  static bool attr_done[64] = {false};
+int mla_tc_clusters() {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMlaSmem) != cudaSuccess)
-      return DCP_ECUDA;
-    attr_done[dev] = true;
+  if (dev < 0 || dev >= 64) return num_sms() / 2 > 0 ? num_sms() / 2 : 1;
+  if (!g_attr_done[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmem);
+    if (e != cudaSuccess) {
+      launch_status_report(e);
+      return -1;
+    }
+    g_attr_done[dev] = true;
   }
-  static int max_clusters[64] = {0};
-  if (dev >= 0 && dev < 64 && max_clusters[dev] == 0) {
+  if (g_clusters[dev] == 0) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
@@ -552,10 +625,36 @@ int launch_mla_tc(const dcp_layout_t& layout, const void* q, int B, int Hq, floa
       cudaGetLastError();
       n = num_sms() / 2;
     }
-    max_clusters[dev] = n;
+    if (n > kMaxParts) n = kMaxParts;
+    g_clusters[dev] = n > 0 ? n : 1;
   }
-  const int clusters = (dev >= 0 && dev < 64) ? max_clusters[dev] : num_sms() / 2;
-  mla_tc_kernel<<<2 * (clusters > 0 ? clusters : 1), kMlaThreads, kMlaSmem, s>>>(A, plan);
+  return g_clusters[dev];
+}
+
+int launch_mla_tc(const dcp_layout_t& layout, const void* q, int B, int Hq, float scale,
+                  const dcp_paged_kv_t& kv, const Plan& plan, int clusters, int32_t* err,
+                  cudaStream_t s) {
+  (void)Hq;
+  if ((uintptr_t)q & 15) return DCP_EUNSUPPORTED;
+  if (clusters < 1 || clusters > kMaxParts) return DCP_EINVAL;
+  MlaTcArgs A;
+  memset(&A, 0, sizeof(A));
+  const uint64_t rows = (uint64_t)kv.num_blocks * layout.block_size;
+  for (int r = 0; r < layout.dcp_size; ++r)
+    if (!encode_2d_bf16_sw128(&A.kvmap[r], kv.k.ptr[r], kDk, rows > 0 ? rows : 1, kDk * 2, 64,
+                              kSt))
+      return DCP_ECUDA;
+  A.q = static_cast<const uint16_t*>(q);
+  A.B = B;
+  A.bs = layout.block_size;
+  A.dcp = layout.dcp_size;
+  A.sl2 = scale * kLog2e;
+  A.bt = kv.block_table;
+  A.max_vb = kv.max_vblocks;
+  A.bt_rank_stride = kv.bt_rank_stride;
+  A.num_blocks = kv.num_blocks;
+  A.err = err;
+  mla_tc_kernel<<<2 * clusters, kMlaThreads, kMlaSmem, s>>>(A, plan);
   return launch_status();
 }
 
