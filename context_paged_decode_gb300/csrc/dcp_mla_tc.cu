@@ -28,7 +28,8 @@
 //  * tensor memory: O half (256 columns) | Q part (128) | two fp32 score
 //    buffers of 64 columns.  P (bf16, 128 x 64) goes to shared memory as the
 //    A operand of P V;
-//  * warp 0 issues TMA (a 3-deep ring of 64-token stages), warp 1 issues
+//  * warp 0 issues TMA (a 3-deep ring of 64-token stages; the tiles three
+//    stages further are prefetched into L2 so a load finds them there), warp 1 issues
 //    Q K^T (up to two stages ahead), warp 2 issues P V, warps 3-10 run the
 //    online softmax: the two warps of one tensor-memory lane quarter take 32
 //    of the 64 columns each and combine their row maxima through shared
@@ -78,13 +79,14 @@ constexpr int kRopeOff = kPOff + kPBytes;              // 200 KB
 constexpr int kMaxOff = kRopeOff + kRopeBytes;         // 216 KB: half-row maxima [2][2][128]
 constexpr int kLsumOff = kMaxOff + 2 * 2 * kHeads * 4; // 218 KB: half-row sums [2][2][128]
 constexpr int kBarOff = kLsumOff + 2 * 2 * kHeads * 4; // 220 KB
-constexpr int kNumBars = 26;
+constexpr int kNumBars = 32;
 constexpr int kMlaSmem = 1024 + kBarOff + kNumBars * 8 + 16;
 constexpr int kSoftWarps = 8;
 constexpr int kFirstSoftWarp = 3;
 constexpr int kMlaThreads = 32 * (kFirstSoftWarp + kSoftWarps);  // 352
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384;
+constexpr int kPrefetch = 3;                           // stages prefetched into L2 ahead of the ring
 constexpr float kRescaleThreshold = 8.f;
 constexpr int kStuckMla = 1 << 20;
 
@@ -107,15 +109,18 @@ enum : int {
   B_O_FREE = 19,
   B_L_FULL = 20,    // +buffer: both halves' row sums of an item are in shared memory
   B_L_FREE = 22,    // +buffer: both halves have read them
-  B_MX_FULL = 24    // +buffer: both halves' row maxima of a stage are in shared memory
+  B_MX_FULL = 24    // +2*quarter+buffer: both halves' row maxima of a stage (one lane quarter)
 };
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kSt, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kDvHalf, false, true);
 
-__device__ __forceinline__ bool counted_by_warps(int i) {
-  return i == B_S_FREE || i == B_S_FREE + 1 || i == B_P_FULL || i == B_X_FREE ||
-         i == B_X_FREE + 1 || i == B_Q_FULL || i == B_O_FREE || i >= B_L_FULL;
+__device__ __forceinline__ int arrivals(int i) {
+  if (i >= B_MX_FULL) return 2;  // the two warps of one lane quarter
+  return (i == B_S_FREE || i == B_S_FREE + 1 || i == B_P_FULL || i == B_X_FREE ||
+          i == B_X_FREE + 1 || i == B_Q_FULL || i == B_O_FREE || i >= B_L_FULL)
+             ? kSoftWarps
+             : 1;
 }
 
 // Eleven warps put three on some SM sub-partitions (16K registers each), so a
@@ -137,7 +142,7 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
   int32_t* errp = A.err ? A.err : plan.hdr + 3;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) mbar_init(bars + 8 * i, counted_by_warps(i) ? kSoftWarps : 1);
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bars + 8 * i, arrivals(i));
     // the receive slots of stages 0 and 1 expect the peer's 32 KB each
     mbar_arrive_expect_tx(bars + 8 * B_X_FULL, kXSlotBytes);
     mbar_arrive_expect_tx(bars + 8 * (B_X_FULL + 1), kXSlotBytes);
@@ -189,6 +194,16 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           } else {
             if (crank == 0) count_error(A.err);
             mbar_arrive(full);
+          }
+          // pull a later stage of this item into L2 so its load above finds it there
+          const int jp = j == 0 ? 1 : j + kPrefetch;
+          for (int jj = jp; jj <= j + kPrefetch && jj < nst; ++jj) {
+            const int64_t pp = bt_phys(b, r, p0, jj);
+            if (pp >= 0 && pp < A.num_blocks) {
+              const int q = p0 + jj * kSt;
+              const int prow = (int)(pp * A.bs + (q - (q / A.bs) * A.bs));
+              for (int c = 0; c < nch; ++c) tma_prefetch_2d(&A.kvmap[r], 64 * (ch0 + c), prow);
+            }
           }
         }
       }
@@ -455,8 +470,8 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
 #pragma unroll
           for (int i = 0; i < w; ++i) t16[i] = fmaxf(t16[i], t16[i + w]);
         hmax[(mb_buf * 2 + hf) * kHeads + head] = t16[0] * A.sl2;
-        warp_arrive(bars + 8 * (B_MX_FULL + mb_buf));
-        if (!wwait(bars + 8 * (B_MX_FULL + mb_buf), (gj >> 1) & 1)) {
+        warp_arrive(bars + 8 * (B_MX_FULL + 2 * q4 + mb_buf));
+        if (!wwait(bars + 8 * (B_MX_FULL + 2 * q4 + mb_buf), (gj >> 1) & 1)) {
           dead = true;
           break;
         }
