@@ -16,26 +16,30 @@
 //    request (its Q stays loaded);
 //  * a cluster of two CTAs per item.  The fp32 output tile 128 x 512 would
 //    fill all of tensor memory, so CTA c keeps value columns [256c, 256c+256).
-//    The 576-wide reduction of Q K^T is split the same way: CTA 0 reduces
-//    over latent columns 0..255, CTA 1 over 256..575 (latent 256..511 plus
-//    the 64 rope columns), and the two fp32 partial score tiles are exchanged
-//    through distributed shared memory and added (IEEE addition commutes, so
-//    both CTAs hold bit-identical scores and take identical decisions);
+//    The 576-wide reduction of Q K^T is split to match: CTA c reduces over
+//    latent columns [256c, 256c+256) and rope columns [512+32c, 544+32c), and
+//    the two fp32 partial score tiles are exchanged through distributed
+//    shared memory and added (IEEE addition commutes, so both CTAs hold
+//    bit-identical scores and take identical decisions);
 //  * a stage is 64 tokens: one tcgen05.mma instruction costs its issuing
 //    thread about as long as an N=64 product takes the tensor core, so Q K^T
-//    runs at N=64 (16 instructions per stage from tensor memory, plus 4 for
-//    the rope chunk, which CTA 1 keeps in shared memory);
+//    runs at N=64 (16 instructions per stage with Q from tensor memory, plus
+//    2 for the rope half, whose Q part sits in shared memory);
 //  * tensor memory: O half (256 columns) | Q part (128) | two fp32 score
-//    buffers of 64 columns.  P (bf16, 128 x 64) goes to shared memory as the
-//    A operand of P V;
-//  * warp 0 issues TMA (a 3-deep ring of 64-token stages; the tiles three
-//    stages further are prefetched into L2 so a load finds them there), warp 1 issues
-//    Q K^T (up to two stages ahead), warp 2 issues P V, warps 3-10 run the
-//    online softmax: the two warps of one tensor-memory lane quarter take 32
-//    of the 64 columns each and combine their row maxima through shared
-//    memory.  A softmax iteration first ships its 32 columns of the next
-//    stage's partial scores to the peer, then finishes the current stage
-//    with the peer's scores, which arrived one iteration ago;
+//    buffers of 64 columns.  Shared memory: a 4-deep ring of 36 KB stages
+//    (64 tokens x 288 columns), two 32 KB receive slots for the peer's
+//    partial scores, and the rope half of Q.  P (bf16, 128 x 64, the A
+//    operand of P V) is written into the receive slot whose scores were just
+//    consumed; the P V that reads it releases the slot to the peer with a
+//    multicast commit;
+//  * warp 0 issues TMA (the tiles three stages beyond the ring are
+//    prefetched into L2), warp 1 issues Q K^T (up to two stages ahead),
+//    warp 2 issues P V, warps 3-10 run the online softmax: the two warps of
+//    one tensor-memory lane quarter take 32 of the 64 columns each and
+//    combine their row maxima through shared memory.  A softmax iteration
+//    adds the peer's partial scores of the current stage (shipped one
+//    iteration ago) to its own, ships its 32 columns of the next stage's
+//    partial scores to the peer, then finishes the current stage;
 //  * the output is rescaled only when the running maximum grows by more
 //    than 8 (log2 units), so P stays <= 256 and the rare rescale waits for
 //    the in-flight P V.
@@ -50,8 +54,9 @@
 namespace dcp {
 
 struct MlaTcArgs {
-  CUtensorMap kvmap[DCP_MAX_RANKS];  // [num_blocks*bs rows][576] bf16, box 64 x 64
-  const uint16_t* q;                 // [B][128][576] bf16
+  CUtensorMap kvmap[DCP_MAX_RANKS];    // [num_blocks*bs rows][576] bf16, box 64 x 64, 128 B swizzle
+  CUtensorMap ropemap[DCP_MAX_RANKS];  // same matrix, box 32 x 64, 64 B swizzle
+  const uint16_t* q;                   // [B][128][576] bf16
   int B, bs, dcp;
   float sl2;
   const int32_t* bt;
@@ -65,21 +70,19 @@ constexpr int kHeads = 128;
 constexpr int kDk = 576;
 constexpr int kDvHalf = 256;
 constexpr int kSt = 64;                                // tokens per stage
-constexpr int kNs = 3;                                 // KV stages in flight
-constexpr int kMaxCh = 5;                              // 64-column chunks per CTA (CTA 1)
+constexpr int kNs = 4;                                 // KV stages in flight
 constexpr int kChunkBytes = kSt * 128;                 // 8 KB: 64 tokens x 64 columns
-constexpr int kStageBytes = kMaxCh * kChunkBytes;      // 40 KB
+constexpr int kRopeTileBytes = kSt * 64;               // 4 KB: 64 tokens x 32 rope columns
+constexpr int kStageBytes = 4 * kChunkBytes + kRopeTileBytes;  // 36 KB
 constexpr int kXSlotBytes = kHeads * kSt * 4;          // 32 KB of fp32 partial scores
-constexpr int kPBytes = kHeads * kSt * 2;              // 16 KB of bf16 P
-constexpr int kRopeBytes = kHeads * 128;               // 16 KB: Q rope chunk (CTA 1)
+constexpr int kQRopeBytes = kHeads * 64;               // 8 KB: this CTA's rope half of Q
 constexpr int kKvOff = 0;
-constexpr int kXOff = kKvOff + kNs * kStageBytes;      // 120 KB
-constexpr int kPOff = kXOff + 2 * kXSlotBytes;         // 184 KB
-constexpr int kRopeOff = kPOff + kPBytes;              // 200 KB
-constexpr int kMaxOff = kRopeOff + kRopeBytes;         // 216 KB: half-row maxima [2][2][128]
+constexpr int kXOff = kKvOff + kNs * kStageBytes;      // 144 KB
+constexpr int kQRopeOff = kXOff + 2 * kXSlotBytes;     // 208 KB
+constexpr int kMaxOff = kQRopeOff + kQRopeBytes;       // 216 KB: half-row maxima [2][2][128]
 constexpr int kLsumOff = kMaxOff + 2 * 2 * kHeads * 4; // 218 KB: half-row sums [2][2][128]
 constexpr int kBarOff = kLsumOff + 2 * 2 * kHeads * 4; // 220 KB
-constexpr int kNumBars = 32;
+constexpr int kNumBars = 29;
 constexpr int kMlaSmem = 1024 + kBarOff + kNumBars * 8 + 16;
 constexpr int kSoftWarps = 8;
 constexpr int kFirstSoftWarp = 3;
@@ -92,33 +95,33 @@ constexpr int kStuckMla = 1 << 20;
 
 static_assert(kColQ + 4 * 32 <= kColS && kColS + 2 * kSt <= kTmemCols, "tensor memory overflow");
 static_assert(kMlaSmem <= 227 * 1024, "shared memory overflow");
+static_assert(kStageBytes % 1024 == 0 && kXSlotBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
 
 // barrier slots
 enum : int {
   B_KV_FULL = 0,    // +stage (kNs)
-  B_KV_EMPTY = 3,   // +stage (kNs)
-  B_S_FULL = 6,     // +score buffer
-  B_S_FREE = 8,     // +score buffer: every softmax warp has read it
-  B_P_FULL = 10,    // every softmax warp has stored its P columns
-  B_P_FREE = 11,    // the P V reading P has completed
-  B_X_FULL = 12,    // +slot: the peer's partial scores landed in my slot
-  B_X_FREE = 14,    // +slot: the peer's softmax warps consumed what I wrote into its slot
-  B_Q_FULL = 16,
-  B_Q_EMPTY = 17,
-  B_O_FULL = 18,
-  B_O_FREE = 19,
-  B_L_FULL = 20,    // +buffer: both halves' row sums of an item are in shared memory
-  B_L_FREE = 22,    // +buffer: both halves have read them
-  B_MX_FULL = 24    // +2*quarter+buffer: both halves' row maxima of a stage (one lane quarter)
+  B_KV_EMPTY = 4,   // +stage (kNs)
+  B_S_FULL = 8,     // +score buffer
+  B_S_FREE = 10,    // +score buffer: every softmax warp has read it
+  B_P_FULL = 12,    // every softmax warp has stored its P columns (one phase per stage)
+  B_PV_DONE = 13,   // the P V of a stage completed (one phase per stage)
+  B_X_FULL = 14,    // +slot: the peer's partial scores landed in my slot
+  B_X_FREE = 16,    // +slot: the peer's P V that read its slot (P) completed
+  B_Q_FULL = 18,
+  B_Q_EMPTY = 19,
+  B_O_FULL = 20,
+  B_O_FREE = 21,
+  B_L_FULL = 22,    // +buffer: both halves' row sums of an item are in shared memory
+  B_L_FREE = 24,    // +buffer: both halves have read them
+  B_MX_FULL = 26    // +buffer: every warp posted its half-row maxima (and finished reading the slot)
 };
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kSt, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kDvHalf, false, true);
 
 __device__ __forceinline__ int arrivals(int i) {
-  if (i >= B_MX_FULL) return 2;  // the two warps of one lane quarter
-  return (i == B_S_FREE || i == B_S_FREE + 1 || i == B_P_FULL || i == B_X_FREE ||
-          i == B_X_FREE + 1 || i == B_Q_FULL || i == B_O_FREE || i >= B_L_FULL)
+  return (i == B_S_FREE || i == B_S_FREE + 1 || i == B_P_FULL || i == B_Q_FULL || i == B_O_FREE ||
+          i >= B_L_FULL)
              ? kSoftWarps
              : 1;
 }
@@ -135,8 +138,6 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();          // 0 or 1: which half this CTA owns
   const uint32_t peer = crank ^ 1u;
-  const int nch = crank == 0 ? 4 : 5;                // 64-column chunks reduced here
-  const int ch0 = crank == 0 ? 0 : 4;                // first global chunk
   const int cl = blockIdx.x >> 1;
   const int i0 = plan.pfirst[cl], i1 = plan.pfirst[cl + 1];
   int32_t* errp = A.err ? A.err : plan.hdr + 3;
@@ -147,7 +148,10 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
     mbar_arrive_expect_tx(bars + 8 * B_X_FULL, kXSlotBytes);
     mbar_arrive_expect_tx(bars + 8 * (B_X_FULL + 1), kXSlotBytes);
     fence_mbar_init();
-    for (int r = 0; r < A.dcp; ++r) prefetch_tmap(&A.kvmap[r]);
+    for (int r = 0; r < A.dcp; ++r) {
+      prefetch_tmap(&A.kvmap[r]);
+      prefetch_tmap(&A.ropemap[r]);
+    }
   }
   if (warp == 1) {
     tc_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -164,11 +168,19 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
     return vb < A.max_vb ? (int64_t)__ldg(A.bt + r * A.bt_rank_stride + (int64_t)b * A.max_vb + vb)
                          : (int64_t)-1;
   };
+  // row of the KV matrix holding local position p0 + j*kSt, -1 if unusable
+  auto stage_row = [&](int b, int r, int p0, int j) -> int {
+    const int64_t phys = bt_phys(b, r, p0, j);
+    if (phys < 0 || phys >= A.num_blocks) return -1;
+    const int p = p0 + j * kSt;
+    return (int)(phys * A.bs + (p - (p / A.bs) * A.bs));
+  };
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
+      const int xlat = 256 * (int)crank, xrope = 512 + 32 * (int)crank;
       uint32_t g = 0;
       bool dead = false;
       for (int it = i0; it < i1 && !dead; ++it) {
@@ -177,32 +189,28 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
         const int nst = (p1 - p0 + kSt - 1) / kSt;
         for (int j = 0; j < nst; ++j, ++g) {
           const uint32_t st = g % kNs, u = g / kNs;
-          const int64_t phys = bt_phys(b, r, p0, j);
+          const int row = stage_row(b, r, p0, j);
           if (!mbar_wait(bars + 8 * (B_KV_EMPTY + st), (u & 1) ^ 1)) {
             dead = true;
             break;
           }
           const uint32_t full = bars + 8 * (B_KV_FULL + st);
-          const int p = p0 + j * kSt;
-          const int off = p - (p / A.bs) * A.bs;
-          if (phys >= 0 && phys < A.num_blocks) {
-            const int row = (int)(phys * A.bs + off);
-            mbar_arrive_expect_tx(full, nch * kChunkBytes);
+          if (row >= 0) {
+            mbar_arrive_expect_tx(full, kStageBytes);
             const uint32_t dst = sbase + kKvOff + st * kStageBytes;
-            for (int c = 0; c < nch; ++c)
-              tma_load_2d_hint(dst + c * kChunkBytes, &A.kvmap[r], 64 * (ch0 + c), row, full, pol);
+            for (int c = 0; c < 4; ++c)
+              tma_load_2d_hint(dst + c * kChunkBytes, &A.kvmap[r], xlat + 64 * c, row, full, pol);
+            tma_load_2d_hint(dst + 4 * kChunkBytes, &A.ropemap[r], xrope, row, full, pol);
           } else {
             if (crank == 0) count_error(A.err);
             mbar_arrive(full);
           }
           // pull a later stage of this item into L2 so its load above finds it there
-          const int jp = j == 0 ? 1 : j + kPrefetch;
-          for (int jj = jp; jj <= j + kPrefetch && jj < nst; ++jj) {
-            const int64_t pp = bt_phys(b, r, p0, jj);
-            if (pp >= 0 && pp < A.num_blocks) {
-              const int q = p0 + jj * kSt;
-              const int prow = (int)(pp * A.bs + (q - (q / A.bs) * A.bs));
-              for (int c = 0; c < nch; ++c) tma_prefetch_2d(&A.kvmap[r], 64 * (ch0 + c), prow);
+          for (int jj = j == 0 ? 1 : j + kPrefetch; jj <= j + kPrefetch && jj < nst; ++jj) {
+            const int prow = stage_row(b, r, p0, jj);
+            if (prow >= 0) {
+              for (int c = 0; c < 4; ++c) tma_prefetch_2d(&A.kvmap[r], xlat + 64 * c, prow);
+              tma_prefetch_2d(&A.ropemap[r], xrope, prow);
             }
           }
         }
@@ -215,7 +223,7 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
       uint32_t g = 0, qv = 0;
       int prev_b = -1;
       bool dead = false;
-      const uint64_t rope_a = sdesc_sw128(sbase + kRopeOff, 0, 1024);
+      const uint64_t qrope_a = sdesc_sw64(sbase + kQRopeOff, 512);
       for (int it = i0; it < i1 && !dead; ++it) {
         const int4 d = plan.item[it];
         const int b = d.x;
@@ -239,7 +247,8 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           }
           tc_fence_after();
           const uint32_t d_s = tmem + kColS + sb * kSt;
-          const uint64_t b0 = sdesc_sw128(sbase + kKvOff + st * kStageBytes, 0, 1024);
+          const uint32_t kv = sbase + kKvOff + st * kStageBytes;
+          const uint64_t b0 = sdesc_sw128(kv, 0, 1024);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -247,12 +256,11 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
               tc_mma_ts(d_s, tmem + kColQ + c * 32 + kk * 8,
                         b0 + (uint64_t)((c * kChunkBytes + kk * 32) >> 4), kIdescQK,
                         (c | kk) != 0);
-          if (nch == 5) {
+          const uint64_t br = sdesc_sw64(kv + 4 * kChunkBytes, 512);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma_ss(d_s, rope_a + (uint64_t)((kk * 32) >> 4),
-                        b0 + (uint64_t)((4 * kChunkBytes + kk * 32) >> 4), kIdescQK, 1u);
-          }
+          for (int kk = 0; kk < 2; ++kk)
+            tc_mma_ss(d_s, qrope_a + (uint64_t)((kk * 32) >> 4), br + (uint64_t)((kk * 32) >> 4),
+                      kIdescQK, 1u);
           tc_commit(bars + 8 * (B_S_FULL + sb));
           if (q_last && j == nst - 1) tc_commit(bars + 8 * B_Q_EMPTY);  // last reader of this Q
         }
@@ -267,12 +275,11 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
     if (lane == 0) {
       uint32_t g = 0, k = 0;
       bool dead = false;
-      const uint64_t p_a = sdesc_sw128(sbase + kPOff, 0, 1024);
       for (int it = i0; it < i1 && !dead; ++it, ++k) {
         const int4 d = plan.item[it];
         const int nst = (d.w - d.z + kSt - 1) / kSt;
         for (int j = 0; j < nst; ++j) {
-          const uint32_t gs = g + j, st = gs % kNs;
+          const uint32_t gs = g + j, st = gs % kNs, sb = gs & 1;
           if (!mbar_wait(bars + 8 * B_P_FULL, gs & 1) ||
               (j == 0 && !mbar_wait(bars + 8 * B_O_FREE, (k & 1) ^ 1))) {
             dead = true;
@@ -281,8 +288,9 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           tc_fence_after();
           // V = this CTA's four value chunks, the MN-major B operand: 64-column
           // atoms kChunkBytes apart, 8-token groups 1024 B apart; k-step kk
-          // starts 16 tokens further.  P is the K-major A operand.
+          // starts 16 tokens further.  P (K-major A operand) is in receive slot sb.
           const uint32_t v = sbase + kKvOff + st * kStageBytes;
+          const uint64_t p_a = sdesc_sw128(sbase + kXOff + sb * kXSlotBytes, 0, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = sdesc_sw128(v + kk * 16 * 128, kChunkBytes, 1024);
@@ -290,7 +298,8 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
                       (j > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(bars + 8 * (B_KV_EMPTY + st));
-          tc_commit(bars + 8 * B_P_FREE);
+          tc_commit(bars + 8 * B_PV_DONE);
+          tc_commit_multicast(bars + 8 * (B_X_FREE + sb), (uint16_t)(1u << peer));
         }
         if (dead) break;
         g += nst;
@@ -310,8 +319,7 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
     const uint32_t xrow = sbase + kXOff + head * 256;      // my row of my receive slots
     const uint32_t xrow_peer = mapa_shared(xrow, peer);    // my row of the peer's slots
     const uint32_t xfull_peer = mapa_shared(bars + 8 * B_X_FULL, peer);
-    const uint32_t xfree_peer = mapa_shared(bars + 8 * B_X_FREE, peer);
-    const uint32_t prow = sbase + kPOff + head * 128;
+    const uint32_t prow = sbase + kXOff + head * 128;      // my row of P (in a receive slot)
     float* hmax = reinterpret_cast<float*>(smem + kMaxOff);  // [2][2][128]
     float* lsum = reinterpret_cast<float*>(smem + kLsumOff);  // [2][2][128]
     uint32_t g = 0, k = 0, qv = 0;
@@ -336,7 +344,7 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
       uint32_t mine[32];
       tc_ld32(tmem + lane_off + kColS + sb * kSt + hf * 32, mine);
       tc_wait_ld(mine);
-      // the peer must have consumed what I put in this slot two stages ago
+      // the peer's slot is free once its P V of two stages ago completed
       if (!__all_sync(0xffffffffu,
                       mbar_wait_relaxed_cluster(bars + 8 * (B_X_FREE + sb), (us & 1) ^ 1)))
         return false;
@@ -375,12 +383,6 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
       }
       // the slot's next phase (stage gs + 2) expects the peer's 32 KB again
       if (armer) mbar_arrive_expect_tx(bars + 8 * (B_X_FULL + sb), kXSlotBytes);
-      // every loaded value feeds `dep`, so the loads complete before the arrival
-      float dep = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) dep += sc[i];
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer + 8 * sb, dep);
       return true;
     };
     for (int it = i0; it < i1 && !dead; ++it, ++k) {
@@ -388,16 +390,16 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
       const int b = d.x, r = d.y & 255, p0 = d.z, p1 = d.w;
       const int nst = (p1 - p0 + kSt - 1) / kSt;
       if (b != prev_b) {
-        // load this half's share of Q row `head`: two 64-column chunks into
-        // tensor memory and (CTA 1) half of the rope chunk into shared memory,
-        // once the previous Q's last Q K^T has completed
+        // load this half's share of Q row `head` (two 64-column latent chunks
+        // into tensor memory, half of the rope half into shared memory) once
+        // the previous Q's last Q K^T has completed
         if (qv > 0 && !wwait(bars + 8 * B_Q_EMPTY, (qv - 1) & 1)) {
           dead = true;
           break;
         }
         tc_fence_after();
         const uint4* src = reinterpret_cast<const uint4*>(
-            A.q + ((int64_t)b * kHeads + head) * kDk + (int64_t)ch0 * 64);
+            A.q + ((int64_t)b * kHeads + head) * kDk + (int64_t)crank * 256);
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
           const int c = 2 * hf + c2;
@@ -412,18 +414,20 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           }
           tc_st32(tmem + lane_off + kColQ + c * 32, v);
         }
-        if (nch == 5) {
-          const uint32_t rrow = sbase + kRopeOff + head * 128;
+        // rope half: 64-byte row `head` of a 64-byte-swizzled tile
+        const uint4* rsrc = reinterpret_cast<const uint4*>(
+            A.q + ((int64_t)b * kHeads + head) * kDk + 512 + 32 * (int64_t)crank);
+        const uint32_t rrow = sbase + kQRopeOff + head * 64;
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int u = hf * 4 + t;
-            const uint4 x = __ldg(src + 4 * 8 + u);
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(rrow + ((u ^ (head & 7)) << 4)),
-                         "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w)
-                         : "memory");
-          }
-          fence_proxy_async_smem();
+        for (int t = 0; t < 2; ++t) {
+          const int u = hf * 2 + t;
+          const uint4 x = __ldg(rsrc + u);
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                           rrow + ((u ^ ((head >> 1) & 3)) << 4)),
+                       "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w)
+                       : "memory");
         }
+        fence_proxy_async_smem();
         tc_wait_st();
         tc_fence_before();
         warp_arrive(bars + 8 * B_Q_FULL);
@@ -440,13 +444,15 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
         break;
       }
       for (int j = 0; j < nst; ++j) {
-        const uint32_t gj = g + j, mb_buf = gj & 1;
-        if (j + 1 < nst && !ship(gj + 1)) {
+        const uint32_t gj = g + j, sb = gj & 1;
+        float sc[32];
+        if (!gather(gj, sc)) {
           dead = true;
           break;
         }
-        float sc[32];
-        if (!gather(gj, sc)) {
+        // ship the next stage now: the peer's slot it goes to is released by
+        // the peer's P V of the previous stage, which is done by this point
+        if (j + 1 < nst && !ship(gj + 1)) {
           dead = true;
           break;
         }
@@ -469,22 +475,22 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
         for (int w = 8; w > 0; w >>= 1)
 #pragma unroll
           for (int i = 0; i < w; ++i) t16[i] = fmaxf(t16[i], t16[i + w]);
-        hmax[(mb_buf * 2 + hf) * kHeads + head] = t16[0] * A.sl2;
-        warp_arrive(bars + 8 * (B_MX_FULL + 2 * q4 + mb_buf));
-        if (!wwait(bars + 8 * (B_MX_FULL + 2 * q4 + mb_buf), (gj >> 1) & 1)) {
+        hmax[(sb * 2 + hf) * kHeads + head] = t16[0] * A.sl2;
+        // every warp has posted its maxima and finished reading the slot
+        warp_arrive(bars + 8 * (B_MX_FULL + sb));
+        if (!wwait(bars + 8 * (B_MX_FULL + sb), (gj >> 1) & 1)) {
           dead = true;
           break;
         }
-        const float mx = fmaxf(hmax[(mb_buf * 2) * kHeads + head],
-                               hmax[(mb_buf * 2 + 1) * kHeads + head]);
-        // P (single buffer) and O are free once the P V of the previous stage completed
-        if (!wwait(bars + 8 * B_P_FREE, (gj & 1) ^ 1)) {
-          dead = true;
-          break;
-        }
+        const float mx = fmaxf(hmax[(sb * 2) * kHeads + head], hmax[(sb * 2 + 1) * kHeads + head]);
         const bool grow = mx > m + kRescaleThreshold;
         const bool need = grow && j > 0 && m > -INFINITY;  // O already holds this row's sums
         if (__any_sync(0xffffffffu, need)) {
+          // wait for the in-flight P V, then rescale this warp's half of the rows that need it
+          if (!wwait(bars + 8 * B_PV_DONE, (gj - 1) & 1)) {
+            dead = true;
+            break;
+          }
           tc_fence_after();
           const float f = need ? exp2f(m - mx) : 1.f;
 #pragma unroll 1
@@ -512,10 +518,12 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           pk[i] = pack_bf16(pa, pq);
         }
         lh += ls;
+        // P goes into the slot just read (every warp is past its reads)
+        const uint32_t pr = prow + sb * kXSlotBytes;
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const int u = hf * 4 + t;
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((u ^ (head & 7)) << 4)),
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(pr + ((u ^ (head & 7)) << 4)),
                        "r"(pk[4 * t]), "r"(pk[4 * t + 1]), "r"(pk[4 * t + 2]), "r"(pk[4 * t + 3])
                        : "memory");
         }
@@ -602,6 +610,20 @@ namespace {
 int g_clusters[64] = {0};
 bool g_attr_done[64] = {false};
 
+// 2-D bf16 map over the latent rows with the given box width and swizzle.
+bool encode_latent(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_cols,
+                   CUtensorMapSwizzle swz) {
+  auto enc = tensor_map_encoder();
+  if (!enc || ((uintptr_t)base & 15) || rows == 0 || rows > (1ull << 32)) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kDk, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kDk * 2};
+  cuuint32_t box[2] = {box_cols, (cuuint32_t)kSt};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool mla_tc_supported(const dcp_layout_t& layout, int B, int Hq, int dk, int dv,
@@ -656,8 +678,10 @@ int launch_mla_tc(const dcp_layout_t& layout, const void* q, int B, int Hq, floa
   memset(&A, 0, sizeof(A));
   const uint64_t rows = (uint64_t)kv.num_blocks * layout.block_size;
   for (int r = 0; r < layout.dcp_size; ++r)
-    if (!encode_2d_bf16_sw128(&A.kvmap[r], kv.k.ptr[r], kDk, rows > 0 ? rows : 1, kDk * 2, 64,
-                              kSt))
+    if (!encode_latent(&A.kvmap[r], kv.k.ptr[r], rows > 0 ? rows : 1, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_latent(&A.ropemap[r], kv.k.ptr[r], rows > 0 ? rows : 1, 32,
+                       CU_TENSOR_MAP_SWIZZLE_64B))
       return DCP_ECUDA;
   A.q = static_cast<const uint16_t*>(q);
   A.B = B;

@@ -386,3 +386,24 @@ __device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t x, int
 }
 
 }  // namespace dcp
+
+namespace dcp {
+
+// Shared-memory matrix descriptor, 64-byte swizzle (rows of 64 bytes, 8-row
+// groups `sbo` apart): layout type 4 at [61,64).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t addr, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
+         (1ull << 46) | (4ull << 61);
+}
+
+// tcgen05.commit that arrives on the barrier at the same shared-memory offset
+// in every CTA of `cta_mask` (bit i = CTA rank i of the cluster).
+__device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+}  // namespace dcp
