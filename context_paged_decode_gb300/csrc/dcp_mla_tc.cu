@@ -28,18 +28,17 @@
 //  * tensor memory: O half (256 columns) | Q part (128) | two fp32 score
 //    buffers of 64 columns.  Shared memory: a 4-deep ring of 36 KB stages
 //    (64 tokens x 288 columns), two 32 KB receive slots for the peer's
-//    partial scores, and the rope half of Q.  P (bf16, 128 x 64, the A
-//    operand of P V) is written into the receive slot whose scores were just
-//    consumed; the P V that reads it releases the slot to the peer with a
-//    multicast commit;
+//    partial scores (each row split over two 16 KB planes of 32 columns),
+//    and the rope half of Q.  P (bf16, 128 x 64, the A operand of P V)
+//    replaces plane 0 of the receive slot whose scores were just consumed,
+//    each row written by the one thread that read it; the P V that reads P
+//    releases the slot to the peer with a multicast commit;
 //  * warp 0 issues TMA (the tiles three stages beyond the ring are
 //    prefetched into L2), warp 1 issues Q K^T (up to two stages ahead),
-//    warp 2 issues P V, warps 3-10 run the online softmax: the two warps of
-//    one tensor-memory lane quarter take 32 of the 64 columns each and
-//    combine their row maxima through shared memory.  A softmax iteration
-//    adds the peer's partial scores of the current stage (shipped one
-//    iteration ago) to its own, ships its 32 columns of the next stage's
-//    partial scores to the peer, then finishes the current stage;
+//    warp 2 issues P V, warps 3-6 ship this CTA's partial scores to the peer
+//    (distributed shared memory moves only ~10 bytes per cycle, so shipping
+//    runs apart from the softmax), warps 7-10 run the online softmax, one
+//    full 64-column head row per thread;
 //  * the output is rescaled only when the running maximum grows by more
 //    than 8 (log2 units), so P stays <= 256 and the rare rescale waits for
 //    the in-flight P V.
@@ -74,18 +73,19 @@ constexpr int kNs = 4;                                 // KV stages in flight
 constexpr int kChunkBytes = kSt * 128;                 // 8 KB: 64 tokens x 64 columns
 constexpr int kRopeTileBytes = kSt * 64;               // 4 KB: 64 tokens x 32 rope columns
 constexpr int kStageBytes = 4 * kChunkBytes + kRopeTileBytes;  // 36 KB
-constexpr int kXSlotBytes = kHeads * kSt * 4;          // 32 KB of fp32 partial scores
+constexpr int kPlaneBytes = kHeads * 128;              // 16 KB: 32 fp32 columns of every row
+constexpr int kXSlotBytes = 2 * kPlaneBytes;           // 32 KB of fp32 partial scores
 constexpr int kQRopeBytes = kHeads * 64;               // 8 KB: this CTA's rope half of Q
 constexpr int kKvOff = 0;
 constexpr int kXOff = kKvOff + kNs * kStageBytes;      // 144 KB
 constexpr int kQRopeOff = kXOff + 2 * kXSlotBytes;     // 208 KB
-constexpr int kMaxOff = kQRopeOff + kQRopeBytes;       // 216 KB: half-row maxima [2][2][128]
-constexpr int kLsumOff = kMaxOff + 2 * 2 * kHeads * 4; // 218 KB: half-row sums [2][2][128]
-constexpr int kBarOff = kLsumOff + 2 * 2 * kHeads * 4; // 220 KB
-constexpr int kNumBars = 29;
+constexpr int kBarOff = kQRopeOff + kQRopeBytes;       // 216 KB
+constexpr int kNumBars = 22;
 constexpr int kMlaSmem = 1024 + kBarOff + kNumBars * 8 + 16;
-constexpr int kSoftWarps = 8;
-constexpr int kFirstSoftWarp = 3;
+constexpr int kShipWarps = 4;
+constexpr int kSoftWarps = 4;
+constexpr int kFirstShipWarp = 3;
+constexpr int kFirstSoftWarp = kFirstShipWarp + kShipWarps;
 constexpr int kMlaThreads = 32 * (kFirstSoftWarp + kSoftWarps);  // 352
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384;
@@ -102,28 +102,24 @@ enum : int {
   B_KV_FULL = 0,    // +stage (kNs)
   B_KV_EMPTY = 4,   // +stage (kNs)
   B_S_FULL = 8,     // +score buffer
-  B_S_FREE = 10,    // +score buffer: every softmax warp has read it
-  B_P_FULL = 12,    // every softmax warp has stored its P columns (one phase per stage)
+  B_S_FREE = 10,    // +score buffer: every shipper and softmax warp has read it
+  B_P_FULL = 12,    // every softmax warp has stored its P rows (one phase per stage)
   B_PV_DONE = 13,   // the P V of a stage completed (one phase per stage)
   B_X_FULL = 14,    // +slot: the peer's partial scores landed in my slot
   B_X_FREE = 16,    // +slot: the peer's P V that read its slot (P) completed
   B_Q_FULL = 18,
   B_Q_EMPTY = 19,
   B_O_FULL = 20,
-  B_O_FREE = 21,
-  B_L_FULL = 22,    // +buffer: both halves' row sums of an item are in shared memory
-  B_L_FREE = 24,    // +buffer: both halves have read them
-  B_MX_FULL = 26    // +buffer: every warp posted its half-row maxima (and finished reading the slot)
+  B_O_FREE = 21
 };
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kSt, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kDvHalf, false, true);
 
 __device__ __forceinline__ int arrivals(int i) {
-  return (i == B_S_FREE || i == B_S_FREE + 1 || i == B_P_FULL || i == B_Q_FULL || i == B_O_FREE ||
-          i >= B_L_FULL)
-             ? kSoftWarps
-             : 1;
+  if (i == B_S_FREE || i == B_S_FREE + 1) return kShipWarps + kSoftWarps;
+  if (i == B_P_FULL || i == B_Q_FULL || i == B_O_FREE) return kSoftWarps;
+  return 1;
 }
 
 // Eleven warps put three on some SM sub-partitions (16K registers each), so a
@@ -174,6 +170,14 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
     if (phys < 0 || phys >= A.num_blocks) return -1;
     const int p = p0 + j * kSt;
     return (int)(phys * A.bs + (p - (p / A.bs) * A.bs));
+  };
+  // tcgen05.ld/st are warp-collective: every wait outcome is made warp-uniform
+  auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(bar, par));
+  };
+  auto warp_arrive = [&](uint32_t bar) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
   };
 
   if (warp == 0) {
@@ -288,7 +292,8 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           tc_fence_after();
           // V = this CTA's four value chunks, the MN-major B operand: 64-column
           // atoms kChunkBytes apart, 8-token groups 1024 B apart; k-step kk
-          // starts 16 tokens further.  P (K-major A operand) is in receive slot sb.
+          // starts 16 tokens further.  P (K-major A operand) is plane 0 of
+          // receive slot sb.
           const uint32_t v = sbase + kKvOff + st * kStageBytes;
           const uint64_t p_a = sdesc_sw128(sbase + kXOff + sb * kXSlotBytes, 0, 1024);
 #pragma unroll
@@ -307,92 +312,74 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
       }
       if (dead) atomicAdd(errp, kStuckMla);
     }
+  } else if (warp < kFirstSoftWarp) {
+    // ---------------- shippers: this CTA's partial scores -> the peer ----------------
+    // Row h of a receive slot is split over two 16 KB planes (columns 0..31,
+    // 32..63), 128 bytes each, 16-byte units swizzled by h & 7.
+    const int q4 = warp & 3;
+    const int head = q4 * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const uint32_t xrow_peer = mapa_shared(sbase + kXOff + head * 128, peer);
+    const uint32_t xfull_peer = mapa_shared(bars + 8 * B_X_FULL, peer);
+    uint32_t g = 0;
+    bool dead = false;
+    for (int it = i0; it < i1 && !dead; ++it) {
+      const int4 d = plan.item[it];
+      const int nst = (d.w - d.z + kSt - 1) / kSt;
+      for (int j = 0; j < nst; ++j) {
+        const uint32_t gs = g + j, sb = gs & 1, us = gs >> 1;
+        if (!wwait(bars + 8 * (B_S_FULL + sb), us & 1)) {
+          dead = true;
+          break;
+        }
+        tc_fence_after();
+        uint32_t s0[32], s1[32];
+        tc_ld32(tmem + lane_off + kColS + sb * kSt, s0);
+        tc_ld32(tmem + lane_off + kColS + sb * kSt + 32, s1);
+        tc_wait_ld(s0);
+        tc_wait_ld(s1);
+        tc_fence_before();
+        warp_arrive(bars + 8 * (B_S_FREE + sb));
+        // the peer's slot is free once its P V of two stages ago completed
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_relaxed_cluster(bars + 8 * (B_X_FREE + sb), (us & 1) ^ 1))) {
+          dead = true;
+          break;
+        }
+        const uint32_t dst = xrow_peer + sb * kXSlotBytes;
+        const uint32_t bar = xfull_peer + 8 * sb;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const uint32_t pu = (uint32_t)((t ^ (head & 7)) << 4);
+          st_async_v4(dst + pu, s0[4 * t], s0[4 * t + 1], s0[4 * t + 2], s0[4 * t + 3], bar);
+          st_async_v4(dst + kPlaneBytes + pu, s1[4 * t], s1[4 * t + 1], s1[4 * t + 2],
+                      s1[4 * t + 3], bar);
+        }
+      }
+      if (dead) break;
+      g += nst;
+    }
+    if (dead && lane == 0) atomicAdd(errp, kStuckMla);
   } else {
-    // ---------------- softmax + epilogue ----------------
-    const int sw = warp - kFirstSoftWarp;    // 0..7
-    const int hf = sw >> 2;                  // which 32 of the 64 stage columns
+    // ---------------- softmax + epilogue (full 64-column rows) ----------------
+    const int sw = warp - kFirstSoftWarp;    // 0..3
     const int q4 = warp & 3;                 // tensor-memory lane quarter of this warp
     const int head = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const int stid = sw * 32 + lane;         // 0..255
+    const int stid = sw * 32 + lane;         // 0..127
     const bool armer = sw == 0 && lane == 0;
-    const uint32_t xrow = sbase + kXOff + head * 256;      // my row of my receive slots
-    const uint32_t xrow_peer = mapa_shared(xrow, peer);    // my row of the peer's slots
-    const uint32_t xfull_peer = mapa_shared(bars + 8 * B_X_FULL, peer);
-    const uint32_t prow = sbase + kXOff + head * 128;      // my row of P (in a receive slot)
-    float* hmax = reinterpret_cast<float*>(smem + kMaxOff);  // [2][2][128]
-    float* lsum = reinterpret_cast<float*>(smem + kLsumOff);  // [2][2][128]
+    const uint32_t xrow = sbase + kXOff + head * 128;      // my row (plane 0) of my receive slots
     uint32_t g = 0, k = 0, qv = 0;
     int prev_b = -1;
     bool dead = false;
-    // tcgen05.ld/st are warp-collective: every wait outcome is made warp-uniform
-    auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(bar, par));
-    };
-    auto wwait_cl = [&](uint32_t bar, uint32_t par) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait_cluster(bar, par));
-    };
-    auto warp_arrive = [&](uint32_t bar) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar);
-    };
-    // ship my 32 columns of this CTA's partial scores of stage gs to the peer
-    auto ship = [&](uint32_t gs) -> bool {
-      const uint32_t sb = gs & 1, us = gs >> 1;
-      if (!wwait(bars + 8 * (B_S_FULL + sb), us & 1)) return false;
-      tc_fence_after();
-      uint32_t mine[32];
-      tc_ld32(tmem + lane_off + kColS + sb * kSt + hf * 32, mine);
-      tc_wait_ld(mine);
-      // the peer's slot is free once its P V of two stages ago completed
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait_relaxed_cluster(bars + 8 * (B_X_FREE + sb), (us & 1) ^ 1)))
-        return false;
-      const uint32_t dst = xrow_peer + sb * kXSlotBytes;
-      const uint32_t bar = xfull_peer + 8 * sb;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int i = hf * 8 + t;  // 16-byte unit of the 256-byte row
-        st_async_v4(dst + ((i ^ (head & 15)) << 4), mine[4 * t], mine[4 * t + 1], mine[4 * t + 2],
-                    mine[4 * t + 3], bar);
-      }
-      return true;
-    };
-    // my 32 columns of the full scores of stage gs: this CTA's partial (read
-    // again from tensor memory, then the buffer is released) plus the peer's
-    auto gather = [&](uint32_t gs, float (&sc)[32]) -> bool {
-      const uint32_t sb = gs & 1, us = gs >> 1;
-      if (!wwait_cl(bars + 8 * (B_X_FULL + sb), us & 1)) return false;
-      uint32_t mine[32];
-      tc_ld32(tmem + lane_off + kColS + sb * kSt + hf * 32, mine);
-      tc_wait_ld(mine);
-      tc_fence_before();
-      warp_arrive(bars + 8 * (B_S_FREE + sb));
-      const uint32_t src = xrow + sb * kXSlotBytes;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int i = hf * 8 + t;
-        uint32_t a, bq, c, d;
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(a), "=r"(bq), "=r"(c), "=r"(d)
-                     : "r"(src + ((i ^ (head & 15)) << 4)));
-        sc[4 * t + 0] = __uint_as_float(mine[4 * t + 0]) + __uint_as_float(a);
-        sc[4 * t + 1] = __uint_as_float(mine[4 * t + 1]) + __uint_as_float(bq);
-        sc[4 * t + 2] = __uint_as_float(mine[4 * t + 2]) + __uint_as_float(c);
-        sc[4 * t + 3] = __uint_as_float(mine[4 * t + 3]) + __uint_as_float(d);
-      }
-      // the slot's next phase (stage gs + 2) expects the peer's 32 KB again
-      if (armer) mbar_arrive_expect_tx(bars + 8 * (B_X_FULL + sb), kXSlotBytes);
-      return true;
-    };
     for (int it = i0; it < i1 && !dead; ++it, ++k) {
       const int4 d = plan.item[it];
       const int b = d.x, r = d.y & 255, p0 = d.z, p1 = d.w;
       const int nst = (p1 - p0 + kSt - 1) / kSt;
       if (b != prev_b) {
-        // load this half's share of Q row `head` (two 64-column latent chunks
-        // into tensor memory, half of the rope half into shared memory) once
-        // the previous Q's last Q K^T has completed
+        // load Q row `head` (four 64-column latent chunks into tensor memory,
+        // the rope half into shared memory) once the previous Q's last Q K^T
+        // has completed
         if (qv > 0 && !wwait(bars + 8 * B_Q_EMPTY, (qv - 1) & 1)) {
           dead = true;
           break;
@@ -400,9 +387,8 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
         tc_fence_after();
         const uint4* src = reinterpret_cast<const uint4*>(
             A.q + ((int64_t)b * kHeads + head) * kDk + (int64_t)crank * 256);
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int c = 2 * hf + c2;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
@@ -419,8 +405,7 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
             A.q + ((int64_t)b * kHeads + head) * kDk + 512 + 32 * (int64_t)crank);
         const uint32_t rrow = sbase + kQRopeOff + head * 64;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int u = hf * 2 + t;
+        for (int u = 0; u < 4; ++u) {
           const uint4 x = __ldg(rsrc + u);
           asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
                            rrow + ((u ^ ((head >> 1) & 3)) << 4)),
@@ -434,59 +419,74 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
         ++qv;
         prev_b = b;
       }
-      float m = -INFINITY, lh = 0.f;
+      float m = -INFINITY, l = 0.f;
       // block-table entries, loaded three stages ahead of use
       int64_t ph[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) ph[i] = i < nst ? bt_phys(b, r, p0, i) : 0;
-      if (nst > 0 && !ship(g)) {
-        dead = true;
-        break;
-      }
       for (int j = 0; j < nst; ++j) {
-        const uint32_t gj = g + j, sb = gj & 1;
-        float sc[32];
-        if (!gather(gj, sc)) {
+        const uint32_t gj = g + j, sb = gj & 1, us = gj >> 1;
+        // full scores of stage gj: this CTA's partial (tensor memory) plus the
+        // peer's (receive slot sb), 64 columns
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(bars + 8 * (B_X_FULL + sb), us & 1))) {
           dead = true;
           break;
         }
-        // ship the next stage now: the peer's slot it goes to is released by
-        // the peer's P V of the previous stage, which is done by this point
-        if (j + 1 < nst && !ship(gj + 1)) {
-          dead = true;
-          break;
+        float sc[64];
+        {
+          uint32_t s0[32], s1[32];
+          tc_ld32(tmem + lane_off + kColS + sb * kSt, s0);
+          tc_ld32(tmem + lane_off + kColS + sb * kSt + 32, s1);
+          tc_wait_ld(s0);
+          tc_wait_ld(s1);
+          tc_fence_before();
+          warp_arrive(bars + 8 * (B_S_FREE + sb));
+          const uint32_t src = xrow + sb * kXSlotBytes;
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const uint32_t pu = (uint32_t)((t ^ (head & 7)) << 4);
+            uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                         : "r"(src + pu));
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(c0), "=r"(c1), "=r"(c2), "=r"(c3)
+                         : "r"(src + kPlaneBytes + pu));
+            sc[4 * t + 0] = __uint_as_float(s0[4 * t + 0]) + __uint_as_float(a0);
+            sc[4 * t + 1] = __uint_as_float(s0[4 * t + 1]) + __uint_as_float(a1);
+            sc[4 * t + 2] = __uint_as_float(s0[4 * t + 2]) + __uint_as_float(a2);
+            sc[4 * t + 3] = __uint_as_float(s0[4 * t + 3]) + __uint_as_float(a3);
+            sc[32 + 4 * t + 0] = __uint_as_float(s1[4 * t + 0]) + __uint_as_float(c0);
+            sc[32 + 4 * t + 1] = __uint_as_float(s1[4 * t + 1]) + __uint_as_float(c1);
+            sc[32 + 4 * t + 2] = __uint_as_float(s1[4 * t + 2]) + __uint_as_float(c2);
+            sc[32 + 4 * t + 3] = __uint_as_float(s1[4 * t + 3]) + __uint_as_float(c3);
+          }
         }
+        // the slot's next phase (stage gj + 2) expects the peer's 32 KB again
+        if (armer) mbar_arrive_expect_tx(bars + 8 * (B_X_FULL + sb), kXSlotBytes);
         const int64_t phj = ph[0];
         ph[0] = ph[1];
         ph[1] = ph[2];
         ph[2] = ph[3];
         if (j + 4 < nst) ph[3] = bt_phys(b, r, p0, j + 4);
         const int nvalid = (phj >= 0 && phj < A.num_blocks) ? min(kSt, p1 - (p0 + j * kSt)) : 0;
-        const int nv = nvalid - hf * 32;     // valid columns among mine
-        // row maximum of my 32 columns (raw scores; the scale is positive)
-        float t16[16];
+        // row maximum (raw scores; the scale is positive)
+        float t32[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = 2 * i < nv ? sc[2 * i] : -INFINITY;
-          const float c = 2 * i + 1 < nv ? sc[2 * i + 1] : -INFINITY;
-          t16[i] = fmaxf(a, c);
+        for (int i = 0; i < 32; ++i) {
+          const float a = 2 * i < nvalid ? sc[2 * i] : -INFINITY;
+          const float c = 2 * i + 1 < nvalid ? sc[2 * i + 1] : -INFINITY;
+          t32[i] = fmaxf(a, c);
         }
 #pragma unroll
-        for (int w = 8; w > 0; w >>= 1)
+        for (int w = 16; w > 0; w >>= 1)
 #pragma unroll
-          for (int i = 0; i < w; ++i) t16[i] = fmaxf(t16[i], t16[i + w]);
-        hmax[(sb * 2 + hf) * kHeads + head] = t16[0] * A.sl2;
-        // every warp has posted its maxima and finished reading the slot
-        warp_arrive(bars + 8 * (B_MX_FULL + sb));
-        if (!wwait(bars + 8 * (B_MX_FULL + sb), (gj >> 1) & 1)) {
-          dead = true;
-          break;
-        }
-        const float mx = fmaxf(hmax[(sb * 2) * kHeads + head], hmax[(sb * 2 + 1) * kHeads + head]);
+          for (int i = 0; i < w; ++i) t32[i] = fmaxf(t32[i], t32[i + w]);
+        const float mx = t32[0] * A.sl2;
         const bool grow = mx > m + kRescaleThreshold;
         const bool need = grow && j > 0 && m > -INFINITY;  // O already holds this row's sums
         if (__any_sync(0xffffffffu, need)) {
-          // wait for the in-flight P V, then rescale this warp's half of the rows that need it
+          // wait for the in-flight P V, then rescale the rows that need it
           if (!wwait(bars + 8 * B_PV_DONE, (gj - 1) & 1)) {
             dead = true;
             break;
@@ -494,9 +494,9 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           tc_fence_after();
           const float f = need ? exp2f(m - mx) : 1.f;
 #pragma unroll 1
-          for (int cc = 0; cc < kDvHalf / 64; ++cc) {
+          for (int cc = 0; cc < kDvHalf / 32; ++cc) {
             uint32_t o[32];
-            const uint32_t ta = tmem + lane_off + kColO + hf * (kDvHalf / 2) + cc * 32;
+            const uint32_t ta = tmem + lane_off + kColO + cc * 32;
             tc_ld32(ta, o);
             tc_wait_ld(o);
 #pragma unroll
@@ -504,29 +504,30 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
             tc_st32(ta, o);
           }
           tc_wait_st();
-          lh *= f;
+          l *= f;
         }
         if (grow) m = mx;
         const float mb = (m == -INFINITY) ? 0.f : m;
+        // P row `head` (64 tokens, bf16) replaces my row of plane 0, which only
+        // this thread read
+        const uint32_t pr = xrow + sb * kXSlotBytes;
         float ls = 0.f;
-        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float pa = 2 * i < nv ? ex2_ftz(fmaf(sc[2 * i], A.sl2, -mb)) : 0.f;
-          const float pq = 2 * i + 1 < nv ? ex2_ftz(fmaf(sc[2 * i + 1], A.sl2, -mb)) : 0.f;
-          ls += pa + pq;
-          pk[i] = pack_bf16(pa, pq);
-        }
-        lh += ls;
-        // P goes into the slot just read (every warp is past its reads)
-        const uint32_t pr = prow + sb * kXSlotBytes;
+        for (int t = 0; t < 8; ++t) {
+          uint32_t pk[4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int u = hf * 4 + t;
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(pr + ((u ^ (head & 7)) << 4)),
-                       "r"(pk[4 * t]), "r"(pk[4 * t + 1]), "r"(pk[4 * t + 2]), "r"(pk[4 * t + 3])
+          for (int e = 0; e < 4; ++e) {
+            const int i = 8 * t + 2 * e;
+            const float pa = i < nvalid ? ex2_ftz(fmaf(sc[i], A.sl2, -mb)) : 0.f;
+            const float pq = i + 1 < nvalid ? ex2_ftz(fmaf(sc[i + 1], A.sl2, -mb)) : 0.f;
+            ls += pa + pq;
+            pk[e] = pack_bf16(pa, pq);
+          }
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(pr + ((t ^ (head & 7)) << 4)),
+                       "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
                        : "memory");
         }
+        l += ls;
         if (nvalid < kSt) {
           // rows past the end may hold anything: zero this CTA's V columns so 0 * x stays 0
           const uint32_t st = gj % kNs;
@@ -549,21 +550,7 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
       }
       if (dead) break;
       g += nst;
-      // epilogue: O / l -> item partial, LSE in natural log.  The row sum is
-      // the sum of the two halves' sums, exchanged through shared memory.
-      const uint32_t lb = k & 1, ul = k >> 1;
-      if (!wwait(bars + 8 * (B_L_FREE + lb), (ul & 1) ^ 1)) {
-        dead = true;
-        break;
-      }
-      lsum[(lb * 2 + hf) * kHeads + head] = lh;
-      warp_arrive(bars + 8 * (B_L_FULL + lb));
-      if (!wwait(bars + 8 * (B_L_FULL + lb), ul & 1)) {
-        dead = true;
-        break;
-      }
-      const float l = lsum[(lb * 2) * kHeads + head] + lsum[(lb * 2 + 1) * kHeads + head];
-      warp_arrive(bars + 8 * (B_L_FREE + lb));
+      // epilogue: O / l -> item partial, LSE in natural log
       if (!wwait(bars + 8 * B_O_FULL, k & 1)) {
         dead = true;
         break;
@@ -571,12 +558,11 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
       tc_fence_after();
       const bool any = l > 0.f;
       const float inv = any ? 1.f / l : 0.f;
-      float* dst = plan.o + ((int64_t)it * kHeads + head) * (2 * kDvHalf) + crank * kDvHalf +
-                   hf * (kDvHalf / 2);
+      float* dst = plan.o + ((int64_t)it * kHeads + head) * (2 * kDvHalf) + crank * kDvHalf;
 #pragma unroll 1
-      for (int cc = 0; cc < kDvHalf / 64; ++cc) {
+      for (int cc = 0; cc < kDvHalf / 32; ++cc) {
         uint32_t o[32];
-        tc_ld32(tmem + lane_off + kColO + hf * (kDvHalf / 2) + cc * 32, o);
+        tc_ld32(tmem + lane_off + kColO + cc * 32, o);
         tc_wait_ld(o);
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
@@ -587,7 +573,7 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           *reinterpret_cast<float4*>(dst + cc * 32 + i) = w;
         }
       }
-      if (crank == 0 && hf == 0)
+      if (crank == 0)
         plan.lse[(int64_t)it * kHeads + head] = any ? (m + log2f(l)) * kLn2 : -INFINITY;
       tc_fence_before();
       warp_arrive(bars + 8 * B_O_FREE);
