@@ -52,7 +52,18 @@ NCU_TRAFFIC = {
                      "sha256_16": "d84b9510e12045c1", "dram_bytes": 1159449344 + 6443264,
                      "kv_bytes": 282732 * 4096,
                      "capture": "profiles/gqa_tma_kernel_gqa_bf16_b32.md"},
+    "mla_bf16_b64": {"source": "context_paged_decode_gb300/csrc/dcp_mla_tc.cu",
+                     "sha256_16": "6d354e5f8fc6c5c3", "dram_bytes": 251985408 + 3456512,
+                     "kv_bytes": 216885 * 1152,
+                     "capture": "profiles/mla_tc_kernel_mla_bf16_b64.md"},
+    "sfa_bf16_b32": {"source": "context_paged_decode_gb300/csrc/dcp_sfa_mma.cu",
+                     "sha256_16": "5e39c310216b018e", "dram_bytes": 78662400 + 4478976,
+                     "kv_bytes": 32 * 2048 * 1152,
+                     "capture": "profiles/sfa_mma_kernel_sfa_bf16_b32.md"},
 }
+# the long-tail workloads run the same kernels
+NCU_TRAFFIC["longtail_gqa"] = NCU_TRAFFIC["gqa_bf16_b32"]
+NCU_TRAFFIC["longtail_mla"] = NCU_TRAFFIC["mla_bf16_b64"]
 
 
 def traffic_per_launch(name, kv_bytes):
