@@ -426,9 +426,10 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
       for (int i = 0; i < 4; ++i) ph[i] = i < nst ? bt_phys(b, r, p0, i) : 0;
       for (int j = 0; j < nst; ++j) {
         const uint32_t gj = g + j, sb = gj & 1, us = gj >> 1;
-        // full scores of stage gj: this CTA's partial (tensor memory) plus the
-        // peer's (receive slot sb), 64 columns
-        if (!__all_sync(0xffffffffu, mbar_wait_cluster(bars + 8 * (B_X_FULL + sb), us & 1))) {
+        // full scores of stage gj: this CTA's partial (tensor memory, once its
+        // Q K^T completed) plus the peer's (receive slot sb), 64 columns
+        if (!wwait(bars + 8 * (B_S_FULL + sb), us & 1) ||
+            !__all_sync(0xffffffffu, mbar_wait_cluster(bars + 8 * (B_X_FULL + sb), us & 1))) {
           dead = true;
           break;
         }
