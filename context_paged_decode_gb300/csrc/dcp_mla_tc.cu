@@ -15,30 +15,43 @@
 //    gets the same number of tokens and consecutive items mostly share a
 //    request (its Q stays loaded);
 //  * a cluster of two CTAs per item.  The fp32 output tile 128 x 512 would
-//    fill all of tensor memory, so CTA c keeps value columns [256c, 256c+256).
-//    The 576-wide reduction of Q K^T is split to match: CTA c reduces over
-//    latent columns [256c, 256c+256) and rope columns [512+32c, 544+32c), and
-//    the two fp32 partial score tiles are exchanged through distributed
-//    shared memory and added (IEEE addition commutes, so both CTAs hold
-//    bit-identical scores and take identical decisions);
+//    fill all of tensor memory, so CTA c keeps value columns [256c, 256c+256)
+//    of every head.  The 576-wide reduction of Q K^T is split to match: CTA c
+//    reduces over latent columns [256c, 256c+256) and rope columns
+//    [512+32c, 544+32c);
+//  * the softmax is split by heads: CTA c owns heads [64c, 64c+64).  Per
+//    stage it receives the peer's fp32 partial scores of those heads (16 KB,
+//    bulk copies), adds its own, runs the online softmax, and sends the bf16 P
+//    rows of its heads (8 KB) plus each head's rescale factor and running
+//    sums back with bulk copies.  Both CTAs then hold all 128 P
+//    rows and run P V on their value half;
 //  * a stage is 64 tokens: one tcgen05.mma instruction costs its issuing
 //    thread about as long as an N=64 product takes the tensor core, so Q K^T
 //    runs at N=64 (16 instructions per stage with Q from tensor memory, plus
 //    2 for the rope half, whose Q part sits in shared memory);
 //  * tensor memory: O half (256 columns) | Q part (128) | two fp32 score
 //    buffers of 64 columns.  Shared memory: a 4-deep ring of 36 KB stages
-//    (64 tokens x 288 columns), two 32 KB receive slots for the peer's
-//    partial scores (each row split over two 16 KB planes of 32 columns),
-//    and the rope half of Q.  P (bf16, 128 x 64, the A operand of P V)
-//    replaces plane 0 of the receive slot whose scores were just consumed,
-//    each row written by the one thread that read it; the P V that reads P
-//    releases the slot to the peer with a multicast commit;
-//  * warp 0 issues TMA (the tiles three stages beyond the ring are
-//    prefetched into L2), warp 1 issues Q K^T (up to two stages ahead),
-//    warp 2 issues P V, warps 3-6 ship this CTA's partial scores to the peer
-//    (distributed shared memory moves only ~10 bytes per cycle, so shipping
-//    runs apart from the softmax), warps 7-10 run the online softmax, one
-//    full 64-column head row per thread;
+//    (64 tokens x 288 columns), a 16 KB receive slot for the peer's partial
+//    scores, a 16 KB staging buffer for the partial scores this CTA sends
+//    (each is refilled once the peer has read the previous stage, early in
+//    its softmax), two 16 KB P tiles (128 rows x 64 bf16, the A operand of
+//    P V), the (factor, sum) side arrays and the rope half of Q;
+//  * warps: 0 issues TMA (the tiles three stages beyond the ring are
+//    prefetched into L2), 1 issues Q K^T, 2 issues P V.  Warps 3-10 each sit
+//    on the tensor-memory lane quarter warp % 4.  On the quarters of the own
+//    heads, two warps run the softmax of each row, one per 32-column half
+//    (the two half-row maxima meet in shared memory).  On the quarters of
+//    the peer's heads, warps 3-6 ship the partial scores and warps 7-10
+//    receive the peer's P: they apply the peer's rescale factors to those
+//    rows of O and write those rows' output.  Shipping stages the scores in
+//    shared memory and sends them with bulk copies: 16-byte remote stores
+//    would fill the SM's memory-instruction path, which the softmax's
+//    shared-memory loads and exp2 instructions also use;
+//  * barrier discipline: a barrier that several warps arrive on either has
+//    each of them wait for the phase they arrived at, or is split by stage
+//    parity so that no warp can arrive for phase n + 1 before phase n has
+//    completed; every parity wait is for a phase at most one ahead of the
+//    last one that waiter observed;
 //  * the output is rescaled only when the running maximum grows by more
 //    than 8 (log2 units), so P stays <= 256 and the rare rescale waits for
 //    the in-flight P V.
@@ -66,6 +79,7 @@ struct MlaTcArgs {
 };
 
 constexpr int kHeads = 128;
+constexpr int kOwn = 64;                               // heads whose softmax a CTA runs
 constexpr int kDk = 576;
 constexpr int kDvHalf = 256;
 constexpr int kSt = 64;                                // tokens per stage
@@ -73,20 +87,25 @@ constexpr int kNs = 4;                                 // KV stages in flight
 constexpr int kChunkBytes = kSt * 128;                 // 8 KB: 64 tokens x 64 columns
 constexpr int kRopeTileBytes = kSt * 64;               // 4 KB: 64 tokens x 32 rope columns
 constexpr int kStageBytes = 4 * kChunkBytes + kRopeTileBytes;  // 36 KB
-constexpr int kPlaneBytes = kHeads * 128;              // 16 KB: 32 fp32 columns of every row
-constexpr int kXSlotBytes = 2 * kPlaneBytes;           // 32 KB of fp32 partial scores
+constexpr int kXsPlane = kOwn * 128;                   // 8 KB: 32 fp32 columns of the own rows
+constexpr int kXsBytes = 2 * kXsPlane;                 // 16 KB of the peer's partial scores
+constexpr int kPtBytes = kHeads * 128;                 // 16 KB: P, 128 rows x 64 bf16
+constexpr int kSideBytes = kOwn * 16;                  // (factor, sum of each half, 0) per own row
+constexpr int kPMsgBytes = kOwn * 128 + kSideBytes;    // what the peer's softmax sends per stage
 constexpr int kQRopeBytes = kHeads * 64;               // 8 KB: this CTA's rope half of Q
 constexpr int kKvOff = 0;
-constexpr int kXOff = kKvOff + kNs * kStageBytes;      // 144 KB
-constexpr int kQRopeOff = kXOff + 2 * kXSlotBytes;     // 208 KB
-constexpr int kBarOff = kQRopeOff + kQRopeBytes;       // 216 KB
-constexpr int kNumBars = 22;
+constexpr int kXsOff = kKvOff + kNs * kStageBytes;     // 144 KB
+constexpr int kStgOff = kXsOff + kXsBytes;             // 160 KB: my partial scores, staged
+constexpr int kPtOff = kStgOff + kXsBytes;             // 176 KB
+constexpr int kQRopeOff = kPtOff + 2 * kPtBytes;       // 208 KB
+constexpr int kSideOwnOff = kQRopeOff + kQRopeBytes;   // 216 KB
+constexpr int kSideRecvOff = kSideOwnOff + 2 * kSideBytes;
+constexpr int kMxOff = kSideRecvOff + 2 * kSideBytes;  // half-row maxima, [sb][half][row]
+constexpr int kBarOff = kMxOff + 2 * 2 * kOwn * 4;      // 221 KB
+constexpr int kNumBars = 30;
 constexpr int kMlaSmem = 1024 + kBarOff + kNumBars * 8 + 16;
-constexpr int kShipWarps = 4;
-constexpr int kSoftWarps = 4;
-constexpr int kFirstShipWarp = 3;
-constexpr int kFirstSoftWarp = kFirstShipWarp + kShipWarps;
-constexpr int kMlaThreads = 32 * (kFirstSoftWarp + kSoftWarps);  // 352
+constexpr int kFirstRowWarp = 3;
+constexpr int kMlaThreads = 32 * (kFirstRowWarp + 8);  // 352
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384;
 constexpr int kPrefetch = 3;                           // stages prefetched into L2 ahead of the ring
@@ -95,30 +114,42 @@ constexpr int kStuckMla = 1 << 20;
 
 static_assert(kColQ + 4 * 32 <= kColS && kColS + 2 * kSt <= kTmemCols, "tensor memory overflow");
 static_assert(kMlaSmem <= 227 * 1024, "shared memory overflow");
-static_assert(kStageBytes % 1024 == 0 && kXSlotBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+static_assert(kNs <= 4, "four barrier slots per ring role");
+static_assert(kStageBytes % 1024 == 0 && kXsOff % 1024 == 0 && kPtOff % 1024 == 0 &&
+                  kQRopeOff % 1024 == 0,
+              "swizzle atoms need 1 KB alignment");
+static_assert(kSideOwnOff % 16 == 0 && kSideRecvOff % 16 == 0, "bulk copies need 16 B alignment");
 
 // barrier slots
 enum : int {
   B_KV_FULL = 0,    // +stage (kNs)
   B_KV_EMPTY = 4,   // +stage (kNs)
   B_S_FULL = 8,     // +score buffer
-  B_S_FREE = 10,    // +score buffer: every shipper and softmax warp has read it
-  B_P_FULL = 12,    // every softmax warp has stored its P rows (one phase per stage)
-  B_PV_DONE = 13,   // the P V of a stage completed (one phase per stage)
-  B_X_FULL = 14,    // +slot: the peer's partial scores landed in my slot
-  B_X_FREE = 16,    // +slot: the peer's P V that read its slot (P) completed
-  B_Q_FULL = 18,
-  B_Q_EMPTY = 19,
-  B_O_FULL = 20,
-  B_O_FREE = 21
+  B_S_FREE = 10,    // +score buffer: the softmax and shipper warps have read it
+  B_P_FULL = 12,    // +stage parity: all 128 P rows of a stage are in place.  Split by
+                    // parity because its arrivals come from two roles, and no role can
+                    // reach stage g + 2 before the P V of stage g has consumed phase g
+  B_X_FULL = 14,    // the peer's partial scores landed in my receive slot (per stage)
+  B_XS_FREE = 16,   // the peer's softmax has read my partial scores (remote arrivals, per stage)
+  B_PT_FREE = 18,   // +tile: the P V of both CTAs that read P tile sb completed.  Every
+                    // role that waits on tile sb's phase for stage g has observed its
+                    // phase for stage g - 2, so a parity wait never aliases
+  B_P_RECV = 20,    // +tile: the peer's P rows and side pairs landed
+  B_Q_FULL = 22,
+  B_Q_EMPTY = 23,
+  B_O_FULL = 24,
+  B_O_FREE = 25,
+  B_MX = 26,        // +own quarter: both halves of its rows stored their maxima (per stage)
+  B_PQ = 28         // +own quarter: both halves of its rows stored P (per stage)
 };
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kSt, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kDvHalf, false, true);
 
 __device__ __forceinline__ int arrivals(int i) {
-  if (i == B_S_FREE || i == B_S_FREE + 1) return kShipWarps + kSoftWarps;
-  if (i == B_P_FULL || i == B_Q_FULL || i == B_O_FREE) return kSoftWarps;
+  if (i == B_S_FREE || i == B_S_FREE + 1 || i == B_O_FREE) return 6;
+  if (i == B_P_FULL || i == B_P_FULL + 1 || i == B_Q_FULL || i == B_XS_FREE) return 4;
+  if (i == B_PT_FREE || i == B_PT_FREE + 1 || (i >= B_MX && i < B_MX + 4)) return 2;
   return 1;
 }
 
@@ -132,7 +163,7 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
   const uint32_t bars = sbase + kBarOff;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kNumBars * 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();          // 0 or 1: which half this CTA owns
+  const uint32_t crank = cluster_ctarank();          // 0 or 1: which halves this CTA owns
   const uint32_t peer = crank ^ 1u;
   const int cl = blockIdx.x >> 1;
   const int i0 = plan.pfirst[cl], i1 = plan.pfirst[cl + 1];
@@ -140,9 +171,10 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) mbar_init(bars + 8 * i, arrivals(i));
-    // the receive slots of stages 0 and 1 expect the peer's 32 KB each
-    mbar_arrive_expect_tx(bars + 8 * B_X_FULL, kXSlotBytes);
-    mbar_arrive_expect_tx(bars + 8 * (B_X_FULL + 1), kXSlotBytes);
+    // the receive slot of stage 0 and the P tiles of stages 0 and 1 expect
+    // the peer's bytes
+    mbar_arrive_expect_tx(bars + 8 * B_X_FULL, kXsBytes);
+    for (int i = 0; i < 2; ++i) mbar_arrive_expect_tx(bars + 8 * (B_P_RECV + i), kPMsgBytes);
     fence_mbar_init();
     for (int r = 0; r < A.dcp; ++r) {
       prefetch_tmap(&A.kvmap[r]);
@@ -158,28 +190,33 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // block-table entry of stage j of an item (-1 beyond the table)
-  auto bt_phys = [&](int b, int r, int p0, int j) -> int64_t {
+  // block-table entry of stage j of an item, as loaded (-1 beyond the
+  // table).  Entries are fetched stages ahead of use and only then widened,
+  // so no instruction waits on the load right after issuing it.
+  auto bt_raw = [&](int b, int r, int p0, int j) -> int32_t {
     const int vb = (p0 + j * kSt) / A.bs;
-    return vb < A.max_vb ? (int64_t)__ldg(A.bt + r * A.bt_rank_stride + (int64_t)b * A.max_vb + vb)
-                         : (int64_t)-1;
+    return vb < A.max_vb ? __ldg(A.bt + r * A.bt_rank_stride + (int64_t)b * A.max_vb + vb) : -1;
   };
-  // row of the KV matrix holding local position p0 + j*kSt, -1 if unusable
-  auto stage_row = [&](int b, int r, int p0, int j) -> int {
-    const int64_t phys = bt_phys(b, r, p0, j);
-    if (phys < 0 || phys >= A.num_blocks) return -1;
+  auto usable = [&](int32_t raw) -> bool { return raw >= 0 && (int64_t)raw < A.num_blocks; };
+  // row of the KV matrix holding local position p0 + j*kSt (raw usable)
+  auto stage_row = [&](int32_t raw, int p0, int j) -> int {
     const int p = p0 + j * kSt;
-    return (int)(phys * A.bs + (p - (p / A.bs) * A.bs));
+    return (int)((int64_t)raw * A.bs + (p - (p / A.bs) * A.bs));
   };
   // tcgen05.ld/st are warp-collective: every wait outcome is made warp-uniform
   auto wwait = [&](uint32_t bar, uint32_t par) -> bool {
     return __all_sync(0xffffffffu, mbar_wait(bar, par));
   };
+  auto cwait = [&](uint32_t bar, uint32_t par) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait_cluster(bar, par));
+  };
+  auto cwait2 = [&](uint32_t a, uint32_t pa, uint32_t b, uint32_t pb) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait2_cluster(a, pa, b, pb));
+  };
   auto warp_arrive = [&](uint32_t bar) {
     __syncwarp();
     if (lane == 0) mbar_arrive(bar);
   };
-
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
@@ -191,15 +228,19 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
         const int4 d = plan.item[it];
         const int b = d.x, r = d.y & 255, p0 = d.z, p1 = d.w;
         const int nst = (p1 - p0 + kSt - 1) / kSt;
+        // raw[i] = block-table entry of stage j + i
+        int32_t raw[kPrefetch + 2];
+#pragma unroll
+        for (int i = 0; i < kPrefetch + 2; ++i) raw[i] = i < nst ? bt_raw(b, r, p0, i) : -1;
         for (int j = 0; j < nst; ++j, ++g) {
           const uint32_t st = g % kNs, u = g / kNs;
-          const int row = stage_row(b, r, p0, j);
           if (!mbar_wait(bars + 8 * (B_KV_EMPTY + st), (u & 1) ^ 1)) {
             dead = true;
             break;
           }
           const uint32_t full = bars + 8 * (B_KV_FULL + st);
-          if (row >= 0) {
+          if (usable(raw[0])) {
+            const int row = stage_row(raw[0], p0, j);
             mbar_arrive_expect_tx(full, kStageBytes);
             const uint32_t dst = sbase + kKvOff + st * kStageBytes;
             for (int c = 0; c < 4; ++c)
@@ -210,13 +251,17 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
             mbar_arrive(full);
           }
           // pull a later stage of this item into L2 so its load above finds it there
-          for (int jj = j == 0 ? 1 : j + kPrefetch; jj <= j + kPrefetch && jj < nst; ++jj) {
-            const int prow = stage_row(b, r, p0, jj);
-            if (prow >= 0) {
+#pragma unroll
+          for (int i = 1; i <= kPrefetch; ++i) {
+            if ((j == 0 || i == kPrefetch) && j + i < nst && usable(raw[i])) {
+              const int prow = stage_row(raw[i], p0, j + i);
               for (int c = 0; c < 4; ++c) tma_prefetch_2d(&A.kvmap[r], xlat + 64 * c, prow);
               tma_prefetch_2d(&A.ropemap[r], xrope, prow);
             }
           }
+#pragma unroll
+          for (int i = 0; i < kPrefetch + 1; ++i) raw[i] = raw[i + 1];
+          raw[kPrefetch + 1] = j + kPrefetch + 2 < nst ? bt_raw(b, r, p0, j + kPrefetch + 2) : -1;
         }
       }
       if (dead) atomicAdd(errp, kStuckMla);
@@ -284,7 +329,7 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
         const int nst = (d.w - d.z + kSt - 1) / kSt;
         for (int j = 0; j < nst; ++j) {
           const uint32_t gs = g + j, st = gs % kNs, sb = gs & 1;
-          if (!mbar_wait(bars + 8 * B_P_FULL, gs & 1) ||
+          if (!mbar_wait(bars + 8 * (B_P_FULL + sb), (gs >> 1) & 1) ||
               (j == 0 && !mbar_wait(bars + 8 * B_O_FREE, (k & 1) ^ 1))) {
             dead = true;
             break;
@@ -292,10 +337,9 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           tc_fence_after();
           // V = this CTA's four value chunks, the MN-major B operand: 64-column
           // atoms kChunkBytes apart, 8-token groups 1024 B apart; k-step kk
-          // starts 16 tokens further.  P (K-major A operand) is plane 0 of
-          // receive slot sb.
+          // starts 16 tokens further.  P (K-major A operand) is P tile sb.
           const uint32_t v = sbase + kKvOff + st * kStageBytes;
-          const uint64_t p_a = sdesc_sw128(sbase + kXOff + sb * kXSlotBytes, 0, 1024);
+          const uint64_t p_a = sdesc_sw128(sbase + kPtOff + sb * kPtBytes, 0, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = sdesc_sw128(v + kk * 16 * 128, kChunkBytes, 1024);
@@ -303,8 +347,8 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
                       (j > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(bars + 8 * (B_KV_EMPTY + st));
-          tc_commit(bars + 8 * B_PV_DONE);
-          tc_commit_multicast(bars + 8 * (B_X_FREE + sb), (uint16_t)(1u << peer));
+          // P tile sb of both CTAs may be rewritten once both P V have read it
+          tc_commit_multicast(bars + 8 * (B_PT_FREE + sb), (uint16_t)3u);
         }
         if (dead) break;
         g += nst;
@@ -312,258 +356,80 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
       }
       if (dead) atomicAdd(errp, kStuckMla);
     }
-  } else if (warp < kFirstSoftWarp) {
-    // ---------------- shippers: this CTA's partial scores -> the peer ----------------
-    // Row h of a receive slot is split over two 16 KB planes (columns 0..31,
-    // 32..63), 128 bytes each, 16-byte units swizzled by h & 7.
-    const int q4 = warp & 3;
-    const int head = q4 * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const uint32_t xrow_peer = mapa_shared(sbase + kXOff + head * 128, peer);
-    const uint32_t xfull_peer = mapa_shared(bars + 8 * B_X_FULL, peer);
-    uint32_t g = 0;
-    bool dead = false;
-    for (int it = i0; it < i1 && !dead; ++it) {
-      const int4 d = plan.item[it];
-      const int nst = (d.w - d.z + kSt - 1) / kSt;
-      for (int j = 0; j < nst; ++j) {
-        const uint32_t gs = g + j, sb = gs & 1, us = gs >> 1;
-        if (!wwait(bars + 8 * (B_S_FULL + sb), us & 1)) {
-          dead = true;
-          break;
-        }
-        tc_fence_after();
-        uint32_t s0[32], s1[32];
-        tc_ld32(tmem + lane_off + kColS + sb * kSt, s0);
-        tc_ld32(tmem + lane_off + kColS + sb * kSt + 32, s1);
-        tc_wait_ld(s0);
-        tc_wait_ld(s1);
-        tc_fence_before();
-        warp_arrive(bars + 8 * (B_S_FREE + sb));
-        // the peer's slot is free once its P V of two stages ago completed
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait_relaxed_cluster(bars + 8 * (B_X_FREE + sb), (us & 1) ^ 1))) {
-          dead = true;
-          break;
-        }
-        const uint32_t dst = xrow_peer + sb * kXSlotBytes;
-        const uint32_t bar = xfull_peer + 8 * sb;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const uint32_t pu = (uint32_t)((t ^ (head & 7)) << 4);
-          st_async_v4(dst + pu, s0[4 * t], s0[4 * t + 1], s0[4 * t + 2], s0[4 * t + 3], bar);
-          st_async_v4(dst + kPlaneBytes + pu, s1[4 * t], s1[4 * t + 1], s1[4 * t + 2],
-                      s1[4 * t + 3], bar);
-        }
-      }
-      if (dead) break;
-      g += nst;
-    }
-    if (dead && lane == 0) atomicAdd(errp, kStuckMla);
   } else {
-    // ---------------- softmax + epilogue (full 64-column rows) ----------------
-    const int sw = warp - kFirstSoftWarp;    // 0..3
-    const int q4 = warp & 3;                 // tensor-memory lane quarter of this warp
+    // ---------------- row warps: one tensor-memory lane (head) per thread ----------------
+    const int q4 = warp & 3;                         // lane quarter = SM sub-partition
     const int head = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const int stid = sw * 32 + lane;         // 0..127
-    const bool armer = sw == 0 && lane == 0;
-    const uint32_t xrow = sbase + kXOff + head * 128;      // my row (plane 0) of my receive slots
-    uint32_t g = 0, k = 0, qv = 0;
-    int prev_b = -1;
-    bool dead = false;
-    for (int it = i0; it < i1 && !dead; ++it, ++k) {
-      const int4 d = plan.item[it];
-      const int b = d.x, r = d.y & 255, p0 = d.z, p1 = d.w;
-      const int nst = (p1 - p0 + kSt - 1) / kSt;
-      if (b != prev_b) {
-        // load Q row `head` (four 64-column latent chunks into tensor memory,
-        // the rope half into shared memory) once the previous Q's last Q K^T
-        // has completed
-        if (qv > 0 && !wwait(bars + 8 * B_Q_EMPTY, (qv - 1) & 1)) {
-          dead = true;
-          break;
-        }
-        tc_fence_after();
-        const uint4* src = reinterpret_cast<const uint4*>(
-            A.q + ((int64_t)b * kHeads + head) * kDk + (int64_t)crank * 256);
+    const bool own = (uint32_t)(q4 >> 1) == crank;   // my softmax heads
+    const bool first_set = warp < kFirstRowWarp + 4;
+    const int hp = (q4 & 1) * 32 + lane;             // row among the 64 heads of its owner
+    const int role = own ? 0 : (first_set ? 1 : 2);  // softmax, ship, receive
+
+    // Q row `head`: four 64-column latent chunks into tensor memory, the rope
+    // half into shared memory; loaded by the softmax and shipper warps (all
+    // four lane quarters) once the previous Q's last Q K^T has completed.
+    auto load_q = [&](int b, uint32_t qv) -> bool {
+      if (qv > 0 && !wwait(bars + 8 * B_Q_EMPTY, (qv - 1) & 1)) return false;
+      tc_fence_after();
+      const uint4* src = reinterpret_cast<const uint4*>(
+          A.q + ((int64_t)b * kHeads + head) * kDk + (int64_t)crank * 256);
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const uint4 x = __ldg(src + c * 8 + t);
-            v[4 * t] = x.x;
-            v[4 * t + 1] = x.y;
-            v[4 * t + 2] = x.z;
-            v[4 * t + 3] = x.w;
-          }
-          tc_st32(tmem + lane_off + kColQ + c * 32, v);
-        }
-        // rope half: 64-byte row `head` of a 64-byte-swizzled tile
-        const uint4* rsrc = reinterpret_cast<const uint4*>(
-            A.q + ((int64_t)b * kHeads + head) * kDk + 512 + 32 * (int64_t)crank);
-        const uint32_t rrow = sbase + kQRopeOff + head * 64;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 x = __ldg(rsrc + u);
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
-                           rrow + ((u ^ ((head >> 1) & 3)) << 4)),
-                       "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w)
-                       : "memory");
-        }
-        fence_proxy_async_smem();
-        tc_wait_st();
-        tc_fence_before();
-        warp_arrive(bars + 8 * B_Q_FULL);
-        ++qv;
-        prev_b = b;
-      }
-      float m = -INFINITY, l = 0.f;
-      // block-table entries, loaded three stages ahead of use
-      int64_t ph[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) ph[i] = i < nst ? bt_phys(b, r, p0, i) : 0;
-      for (int j = 0; j < nst; ++j) {
-        const uint32_t gj = g + j, sb = gj & 1, us = gj >> 1;
-        // full scores of stage gj: this CTA's partial (tensor memory, once its
-        // Q K^T completed) plus the peer's (receive slot sb), 64 columns
-        if (!wwait(bars + 8 * (B_S_FULL + sb), us & 1) ||
-            !__all_sync(0xffffffffu, mbar_wait_cluster(bars + 8 * (B_X_FULL + sb), us & 1))) {
-          dead = true;
-          break;
-        }
-        float sc[64];
-        {
-          uint32_t s0[32], s1[32];
-          tc_ld32(tmem + lane_off + kColS + sb * kSt, s0);
-          tc_ld32(tmem + lane_off + kColS + sb * kSt + 32, s1);
-          tc_wait_ld(s0);
-          tc_wait_ld(s1);
-          tc_fence_before();
-          warp_arrive(bars + 8 * (B_S_FREE + sb));
-          const uint32_t src = xrow + sb * kXSlotBytes;
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const uint32_t pu = (uint32_t)((t ^ (head & 7)) << 4);
-            uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                         : "r"(src + pu));
-            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(c0), "=r"(c1), "=r"(c2), "=r"(c3)
-                         : "r"(src + kPlaneBytes + pu));
-            sc[4 * t + 0] = __uint_as_float(s0[4 * t + 0]) + __uint_as_float(a0);
-            sc[4 * t + 1] = __uint_as_float(s0[4 * t + 1]) + __uint_as_float(a1);
-            sc[4 * t + 2] = __uint_as_float(s0[4 * t + 2]) + __uint_as_float(a2);
-            sc[4 * t + 3] = __uint_as_float(s0[4 * t + 3]) + __uint_as_float(a3);
-            sc[32 + 4 * t + 0] = __uint_as_float(s1[4 * t + 0]) + __uint_as_float(c0);
-            sc[32 + 4 * t + 1] = __uint_as_float(s1[4 * t + 1]) + __uint_as_float(c1);
-            sc[32 + 4 * t + 2] = __uint_as_float(s1[4 * t + 2]) + __uint_as_float(c2);
-            sc[32 + 4 * t + 3] = __uint_as_float(s1[4 * t + 3]) + __uint_as_float(c3);
-          }
-        }
-        // the slot's next phase (stage gj + 2) expects the peer's 32 KB again
-        if (armer) mbar_arrive_expect_tx(bars + 8 * (B_X_FULL + sb), kXSlotBytes);
-        const int64_t phj = ph[0];
-        ph[0] = ph[1];
-        ph[1] = ph[2];
-        ph[2] = ph[3];
-        if (j + 4 < nst) ph[3] = bt_phys(b, r, p0, j + 4);
-        const int nvalid = (phj >= 0 && phj < A.num_blocks) ? min(kSt, p1 - (p0 + j * kSt)) : 0;
-        // row maximum (raw scores; the scale is positive)
-        float t32[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float a = 2 * i < nvalid ? sc[2 * i] : -INFINITY;
-          const float c = 2 * i + 1 < nvalid ? sc[2 * i + 1] : -INFINITY;
-          t32[i] = fmaxf(a, c);
-        }
-#pragma unroll
-        for (int w = 16; w > 0; w >>= 1)
-#pragma unroll
-          for (int i = 0; i < w; ++i) t32[i] = fmaxf(t32[i], t32[i + w]);
-        const float mx = t32[0] * A.sl2;
-        const bool grow = mx > m + kRescaleThreshold;
-        const bool need = grow && j > 0 && m > -INFINITY;  // O already holds this row's sums
-        if (__any_sync(0xffffffffu, need)) {
-          // wait for the in-flight P V, then rescale the rows that need it
-          if (!wwait(bars + 8 * B_PV_DONE, (gj - 1) & 1)) {
-            dead = true;
-            break;
-          }
-          tc_fence_after();
-          const float f = need ? exp2f(m - mx) : 1.f;
-#pragma unroll 1
-          for (int cc = 0; cc < kDvHalf / 32; ++cc) {
-            uint32_t o[32];
-            const uint32_t ta = tmem + lane_off + kColO + cc * 32;
-            tc_ld32(ta, o);
-            tc_wait_ld(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-            tc_st32(ta, o);
-          }
-          tc_wait_st();
-          l *= f;
-        }
-        if (grow) m = mx;
-        const float mb = (m == -INFINITY) ? 0.f : m;
-        // P row `head` (64 tokens, bf16) replaces my row of plane 0, which only
-        // this thread read
-        const uint32_t pr = xrow + sb * kXSlotBytes;
-        float ls = 0.f;
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-          uint32_t pk[4];
+          const uint4 x = __ldg(src + c * 8 + t);
+          v[4 * t] = x.x;
+          v[4 * t + 1] = x.y;
+          v[4 * t + 2] = x.z;
+          v[4 * t + 3] = x.w;
+        }
+        tc_st32(tmem + lane_off + kColQ + c * 32, v);
+      }
+      // rope half: 64-byte row `head` of a 64-byte-swizzled tile
+      const uint4* rsrc = reinterpret_cast<const uint4*>(
+          A.q + ((int64_t)b * kHeads + head) * kDk + 512 + 32 * (int64_t)crank);
+      const uint32_t rrow = sbase + kQRopeOff + head * 64;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = 8 * t + 2 * e;
-            const float pa = i < nvalid ? ex2_ftz(fmaf(sc[i], A.sl2, -mb)) : 0.f;
-            const float pq = i + 1 < nvalid ? ex2_ftz(fmaf(sc[i + 1], A.sl2, -mb)) : 0.f;
-            ls += pa + pq;
-            pk[e] = pack_bf16(pa, pq);
-          }
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(pr + ((t ^ (head & 7)) << 4)),
-                       "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
-                       : "memory");
-        }
-        l += ls;
-        if (nvalid < kSt) {
-          // rows past the end may hold anything: zero this CTA's V columns so 0 * x stays 0
-          const uint32_t st = gj % kNs;
-          if (!wwait(bars + 8 * (B_KV_FULL + st), (gj / kNs) & 1)) {
-            dead = true;
-            break;
-          }
-          const uint32_t v = sbase + kKvOff + st * kStageBytes;
-          const int total = (kSt - nvalid) * 4 * 8;
-          for (int i = stid; i < total; i += 32 * kSoftWarps) {
-            const int rr = nvalid + (i >> 5), ch = (i >> 3) & 3, part = i & 7;
-            asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
-                             v + ch * kChunkBytes + rr * 128 + part * 16),
-                         "r"(0u)
-                         : "memory");
-          }
-        }
-        fence_proxy_async_smem();   // P and zeroed V rows are read by the tensor core
-        warp_arrive(bars + 8 * B_P_FULL);
+      for (int u = 0; u < 4; ++u) {
+        const uint4 x = __ldg(rsrc + u);
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                         rrow + ((u ^ ((head >> 1) & 3)) << 4)),
+                     "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w)
+                     : "memory");
       }
-      if (dead) break;
-      g += nst;
-      // epilogue: O / l -> item partial, LSE in natural log
-      if (!wwait(bars + 8 * B_O_FULL, k & 1)) {
-        dead = true;
-        break;
+      fence_proxy_async_smem();
+      tc_wait_st();
+      tc_fence_before();
+      warp_arrive(bars + 8 * B_Q_FULL);
+      return true;
+    };
+    // multiply columns [c0, c0 + 32 nc) of row `head` of the O half by f
+    // (after the in-flight P V)
+    auto rescale_o = [&](float f, int c0, int nc) {
+#pragma unroll 1
+      for (int cc = 0; cc < nc; ++cc) {
+        uint32_t o[32];
+        const uint32_t ta = tmem + lane_off + kColO + c0 + cc * 32;
+        tc_ld32(ta, o);
+        tc_wait_ld(o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+        tc_st32(ta, o);
       }
-      tc_fence_after();
+      tc_wait_st();
+    };
+    // columns [c0, c0 + 32 nc) of O half row `head`, / l -> item partial
+    auto write_o = [&](int it, float l, int c0, int nc) {
       const bool any = l > 0.f;
       const float inv = any ? 1.f / l : 0.f;
-      float* dst = plan.o + ((int64_t)it * kHeads + head) * (2 * kDvHalf) + crank * kDvHalf;
+      float* dst =
+          plan.o + ((int64_t)it * kHeads + head) * (2 * kDvHalf) + crank * kDvHalf + c0;
 #pragma unroll 1
-      for (int cc = 0; cc < kDvHalf / 32; ++cc) {
+      for (int cc = 0; cc < nc; ++cc) {
         uint32_t o[32];
-        tc_ld32(tmem + lane_off + kColO + cc * 32, o);
+        tc_ld32(tmem + lane_off + kColO + c0 + cc * 32, o);
         tc_wait_ld(o);
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
@@ -574,12 +440,337 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           *reinterpret_cast<float4*>(dst + cc * 32 + i) = w;
         }
       }
-      if (crank == 0)
-        plan.lse[(int64_t)it * kHeads + head] = any ? (m + log2f(l)) * kLn2 : -INFINITY;
-      tc_fence_before();
-      warp_arrive(bars + 8 * B_O_FREE);
+    };
+
+    if (role == 1) {
+      // ---------- shipper: partial scores of the peer's heads -> the peer ----------
+      // Row hp of a receive slot is split over two 8 KB planes (columns
+      // 0..31, 32..63), 128 bytes each, 16-byte units swizzled by hp & 7.
+      // The rows are staged in the same layout in this CTA and sent with two
+      // 4 KB bulk copies per warp: remote 16-byte stores would queue in the
+      // SM's memory-instruction path that the softmax shares.
+      const uint32_t srow = sbase + kStgOff + hp * 128;
+      const uint32_t half_off = (uint32_t)(q4 & 1) * 4096;
+      const uint32_t xs_peer = mapa_shared(sbase + kXsOff + half_off, peer);
+      const uint32_t xfull_peer = mapa_shared(bars + 8 * B_X_FULL, peer);
+      uint32_t g = 0, qv = 0;
+      int prev_b = -1;
+      bool dead = false;
+      for (int it = i0; it < i1 && !dead; ++it) {
+        const int4 d = plan.item[it];
+        const int nst = (d.w - d.z + kSt - 1) / kSt;
+        if (d.x != prev_b) {
+          if (!load_q(d.x, qv)) {
+            dead = true;
+            break;
+          }
+          ++qv;
+          prev_b = d.x;
+        }
+        for (int j = 0; j < nst; ++j) {
+          const uint32_t gs = g + j, sb = gs & 1, us = gs >> 1;
+          if (!wwait(bars + 8 * (B_S_FULL + sb), us & 1)) {
+            dead = true;
+            break;
+          }
+          tc_fence_after();
+          uint32_t s0[32], s1[32];
+          tc_ld32(tmem + lane_off + kColS + sb * kSt, s0);
+          tc_ld32(tmem + lane_off + kColS + sb * kSt + 32, s1);
+          tc_wait_ld(s0);
+          tc_wait_ld(s1);
+          tc_fence_before();
+          warp_arrive(bars + 8 * (B_S_FREE + sb));
+          // the staging buffer and the peer's slot are free once the peer's
+          // softmax read stage gs - 1 (which the copy from this buffer filled)
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait_relaxed_cluster(bars + 8 * B_XS_FREE, (gs & 1) ^ 1))) {
+            dead = true;
+            break;
+          }
+          const uint32_t dst = srow;
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const uint32_t pu = (uint32_t)((t ^ (hp & 7)) << 4);
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst + pu), "r"(s0[4 * t]),
+                         "r"(s0[4 * t + 1]), "r"(s0[4 * t + 2]), "r"(s0[4 * t + 3])
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst + kXsPlane + pu),
+                         "r"(s1[4 * t]), "r"(s1[4 * t + 1]), "r"(s1[4 * t + 2]),
+                         "r"(s1[4 * t + 3])
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t src = sbase + kStgOff + half_off;
+            bulk_copy_cluster(xs_peer, src, 4096, xfull_peer);
+            bulk_copy_cluster(xs_peer + kXsPlane, src + kXsPlane, 4096, xfull_peer);
+          }
+        }
+        if (dead) break;
+        g += nst;
+      }
+      if (dead && lane == 0) atomicAdd(errp, kStuckMla);
+    } else if (role == 2) {
+      // ---------- receiver: the peer's P rows for its heads ----------
+      const uint32_t side = sbase + kSideRecvOff + hp * 16;
+      const bool armer = lane == 0 && (q4 & 1) == 0;
+      uint32_t g = 0, k = 0;
+      bool dead = false;
+      for (int it = i0; it < i1 && !dead; ++it, ++k) {
+        const int4 d = plan.item[it];
+        const int nst = (d.w - d.z + kSt - 1) / kSt;
+        float lr = 0.f;
+        for (int j = 0; j < nst; ++j) {
+          const uint32_t gj = g + j, sb = gj & 1, us = gj >> 1;
+          // the peer's P rows of stage gj; and P tile sb's phase for stage gj - 2,
+          // observed so that the rescale wait of stage gj + 1 cannot alias
+          if (!cwait2(bars + 8 * (B_P_RECV + sb), us & 1, bars + 8 * (B_PT_FREE + sb),
+                      (us & 1) ^ 1)) {
+            dead = true;
+            break;
+          }
+          // side entry: (f, l of half 0, l of half 1, -)
+          float f, l0, l1;
+          asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];"
+                       : "=f"(f), "=f"(l0)
+                       : "r"(side + sb * kSideBytes));
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l1) : "r"(side + sb * kSideBytes + 8));
+          lr = l0 + l1;
+          // the tile's next phase (stage gj + 2) expects the peer's bytes again
+          if (armer) mbar_arrive_expect_tx_relaxed(bars + 8 * (B_P_RECV + sb), kPMsgBytes);
+          if (__any_sync(0xffffffffu, f != 1.f)) {
+            // wait for the P V of stage gj - 1 (in both CTAs), then rescale
+            if (!cwait(bars + 8 * (B_PT_FREE + ((gj - 1) & 1)), ((gj - 1) >> 1) & 1)) {
+              dead = true;
+              break;
+            }
+            tc_fence_after();
+            rescale_o(f, 0, kDvHalf / 32);
+          }
+          tc_fence_before();
+          warp_arrive(bars + 8 * (B_P_FULL + sb));
+        }
+        if (dead) break;
+        g += nst;
+        if (!wwait(bars + 8 * B_O_FULL, k & 1)) {
+          dead = true;
+          break;
+        }
+        tc_fence_after();
+        write_o(it, lr, 0, kDvHalf / 32);
+        tc_fence_before();
+        warp_arrive(bars + 8 * B_O_FREE);
+      }
+      if (dead && lane == 0) atomicAdd(errp, kStuckMla);
+    } else {
+      // ---------- softmax of the own heads: one 32-column half of a row per thread ----------
+      const int h = first_set ? 0 : 1;               // which half of the 64 columns
+      const int qo = q4 & 1;                         // which own quarter
+      const int stid = h * 64 + qo * 32 + lane;      // 0..127
+      const bool lead = lane == 0;
+      const bool armer = lead && h == 0 && qo == 0;
+      const uint32_t xrow = sbase + kXsOff + h * kXsPlane + hp * 128;  // my half-row of the slots
+      const uint32_t prow = sbase + kPtOff + head * 128;               // my row of the P tiles
+      const uint32_t side = sbase + kSideOwnOff + hp * 16;
+      const uint32_t mx_mine = sbase + kMxOff + (h * kOwn + hp) * 4;
+      const uint32_t mx_other = sbase + kMxOff + ((1 - h) * kOwn + hp) * 4;
+      const uint32_t mxbar = bars + 8 * (B_MX + qo), pqbar = bars + 8 * (B_PQ + qo);
+      const uint32_t xsfree_peer = mapa_shared(bars + 8 * B_XS_FREE, peer);
+      const uint32_t precv_peer = mapa_shared(bars + 8 * B_P_RECV, peer);
+      const uint32_t pt_peer = mapa_shared(sbase + kPtOff + q4 * 4096, peer);
+      const uint32_t side_peer = mapa_shared(sbase + kSideRecvOff + qo * 512, peer);
+      uint32_t g = 0, k = 0, qv = 0;
+      int prev_b = -1;
+      bool dead = false;
+      for (int it = i0; it < i1 && !dead; ++it, ++k) {
+        const int4 d = plan.item[it];
+        const int b = d.x, r = d.y & 255, p0 = d.z, p1 = d.w;
+        const int nst = (p1 - p0 + kSt - 1) / kSt;
+        if (b != prev_b) {
+          if (h == 0 && !load_q(b, qv)) {
+            dead = true;
+            break;
+          }
+          ++qv;
+          prev_b = b;
+        }
+        float m = -INFINITY, lh = 0.f;
+        // block-table entries, loaded three stages ahead of use
+        int32_t ph[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ph[i] = i < nst ? bt_raw(b, r, p0, i) : -1;
+        uint32_t sb_last = 0;
+        for (int j = 0; j < nst; ++j) {
+          const uint32_t gj = g + j, sb = gj & 1, us = gj >> 1;
+          sb_last = sb;
+          const int32_t phj = ph[0];
+          ph[0] = ph[1];
+          ph[1] = ph[2];
+          ph[2] = ph[3];
+          if (j + 4 < nst) ph[3] = bt_raw(b, r, p0, j + 4);
+          const int nvalid = usable(phj) ? min(kSt, p1 - (p0 + j * kSt)) : 0;
+          const int nv = nvalid - 32 * h;            // valid columns of my half (may be <= 0)
+          // full scores of my half of stage gj: this CTA's partial (tensor
+          // memory) plus the peer's (receive slot sb), 32 columns
+          if (!cwait2(bars + 8 * (B_S_FULL + sb), us & 1, bars + 8 * B_X_FULL, gj & 1)) {
+            dead = true;
+            break;
+          }
+          tc_fence_after();
+          float sc[32];
+          {
+            uint32_t s0[32];
+            tc_ld32(tmem + lane_off + kColS + sb * kSt + 32 * h, s0);
+            tc_wait_ld(s0);
+            tc_fence_before();
+            warp_arrive(bars + 8 * (B_S_FREE + sb));
+            const uint32_t src = xrow;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const uint32_t pu = (uint32_t)((t ^ (hp & 7)) << 4);
+              uint32_t a0, a1, a2, a3;
+              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                           : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                           : "r"(src + pu));
+              sc[4 * t + 0] = __uint_as_float(s0[4 * t + 0]) + __uint_as_float(a0);
+              sc[4 * t + 1] = __uint_as_float(s0[4 * t + 1]) + __uint_as_float(a1);
+              sc[4 * t + 2] = __uint_as_float(s0[4 * t + 2]) + __uint_as_float(a2);
+              sc[4 * t + 3] = __uint_as_float(s0[4 * t + 3]) + __uint_as_float(a3);
+            }
+          }
+          // the slot's next phase (stage gj + 1) expects the peer's 16 KB again
+          if (armer) mbar_arrive_expect_tx_relaxed(bars + 8 * B_X_FULL, kXsBytes);
+          // half-row maximum (raw scores; the scale is positive)
+          float t16[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a = 2 * i < nv ? sc[2 * i] : -INFINITY;
+            const float c = 2 * i + 1 < nv ? sc[2 * i + 1] : -INFINITY;
+            t16[i] = fmaxf(a, c);
+          }
+#pragma unroll
+          for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) t16[i] = fmaxf(t16[i], t16[i + w]);
+          // every lane's slot reads are complete once the vote has all maxima:
+          // the vote result orders the remote arrival after them
+          {
+            const uint32_t vote = __ballot_sync(0xffffffffu, t16[0] > 0.f);
+            if (lead) mbar_arrive_remote_relaxed(xsfree_peer, __uint_as_float(vote));
+          }
+          // the row maximum: exchange the half-row maxima with the other half
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(mx_mine + sb * (2 * kOwn * 4)),
+                       "f"(t16[0])
+                       : "memory");
+          warp_arrive(mxbar);
+          // also P tile sb: free once the P V of stage gj - 2 completed in both CTAs
+          if (!cwait2(mxbar, gj & 1, bars + 8 * (B_PT_FREE + sb), (us & 1) ^ 1)) {
+            dead = true;
+            break;
+          }
+          float mo;
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(mo) : "r"(mx_other + sb * (2 * kOwn * 4)));
+          const float mx = fmaxf(t16[0], mo) * A.sl2;
+          const bool grow = mx > m + kRescaleThreshold;
+          const bool need = grow && j > 0 && m > -INFINITY;  // O already holds this row's sums
+          float f = 1.f;
+          if (__any_sync(0xffffffffu, need)) {
+            // wait for the P V of stage gj - 1 (in both CTAs), then rescale my
+            // half of the rows that need it
+            if (!cwait(bars + 8 * (B_PT_FREE + ((gj - 1) & 1)), ((gj - 1) >> 1) & 1)) {
+              dead = true;
+              break;
+            }
+            tc_fence_after();
+            if (need) f = exp2f(m - mx);
+            rescale_o(f, h * (kDvHalf / 2), kDvHalf / 64);
+          }
+          if (grow) m = mx;
+          const float mb = (m == -INFINITY) ? 0.f : m;
+          // my half of P row `head` (32 tokens, bf16)
+          uint32_t pk[16];
+          float ls = 0.f;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int i = 2 * e;
+            const float pa = i < nv ? ex2_ftz(fmaf(sc[i], A.sl2, -mb)) : 0.f;
+            const float pq = i + 1 < nv ? ex2_ftz(fmaf(sc[i + 1], A.sl2, -mb)) : 0.f;
+            ls += pa + pq;
+            pk[e] = pack_bf16(pa, pq);
+          }
+          lh = lh * f + ls;
+          const uint32_t pr = prow + sb * kPtBytes;
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                             pr + (((4 * h + t) ^ (head & 7)) << 4)),
+                         "r"(pk[4 * t]), "r"(pk[4 * t + 1]), "r"(pk[4 * t + 2]), "r"(pk[4 * t + 3])
+                         : "memory");
+          if (h == 0)
+            asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(side + sb * kSideBytes), "f"(f),
+                         "f"(lh)
+                         : "memory");
+          else
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(side + sb * kSideBytes + 8), "f"(lh)
+                         : "memory");
+          if (nvalid < kSt) {
+            // rows past the end may hold anything: zero this CTA's V columns so 0 * x stays 0
+            const uint32_t st = gj % kNs;
+            if (!wwait(bars + 8 * (B_KV_FULL + st), (gj / kNs) & 1)) {
+              dead = true;
+              break;
+            }
+            const uint32_t v = sbase + kKvOff + st * kStageBytes;
+            const int total = (kSt - nvalid) * 4 * 8;
+            for (int i = stid; i < total; i += 2 * kOwn) {
+              const int rr = nvalid + (i >> 5), ch = (i >> 3) & 3, part = i & 7;
+              asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
+                               v + ch * kChunkBytes + rr * 128 + part * 16),
+                           "r"(0u)
+                           : "memory");
+            }
+          }
+          fence_proxy_async_smem();   // P, the side values and zeroed V rows are read asynchronously
+          warp_arrive(pqbar);
+          if (!wwait(pqbar, gj & 1)) {
+            dead = true;
+            break;
+          }
+          if (h == 0 && lead) {
+            // these 32 P rows and side entries -> the same places in the peer
+            bulk_copy_cluster(pt_peer + sb * kPtBytes, sbase + kPtOff + sb * kPtBytes + q4 * 4096,
+                              4096, precv_peer + 8 * sb);
+            bulk_copy_cluster(side_peer + sb * kSideBytes,
+                              sbase + kSideOwnOff + sb * kSideBytes + qo * 512, 512,
+                              precv_peer + 8 * sb);
+            mbar_arrive(bars + 8 * (B_P_FULL + sb));
+          }
+        }
+        if (dead) break;
+        g += nst;
+        // epilogue: my half of O / l -> item partial, LSE in natural log
+        if (!wwait(bars + 8 * B_O_FULL, k & 1)) {
+          dead = true;
+          break;
+        }
+        tc_fence_after();
+        // side entry of the last stage: (f, l of half 0, l of half 1, -)
+        float l0 = 0.f, l1 = 0.f;
+        if (nst > 0) {
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l0) : "r"(side + sb_last * kSideBytes + 4));
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l1) : "r"(side + sb_last * kSideBytes + 8));
+        }
+        const float l = l0 + l1;
+        write_o(it, l, h * (kDvHalf / 2), kDvHalf / 64);
+        if (h == 0)
+          plan.lse[(int64_t)it * kHeads + head] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        tc_fence_before();
+        warp_arrive(bars + 8 * B_O_FREE);
+      }
+      if (dead && lane == 0) atomicAdd(errp, kStuckMla);
     }
-    if (dead && lane == 0) atomicAdd(errp, kStuckMla);
   }
   tc_fence_before();
   __syncthreads();

@@ -407,3 +407,49 @@ __device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t cta_m
 }
 
 }  // namespace dcp
+
+namespace dcp {
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory into another CTA's of the cluster; the bytes
+// complete on that CTA's mbarrier `bar_cluster`.
+__device__ __forceinline__ void bulk_copy_cluster(uint32_t dst_cluster, uint32_t src,
+                                                  uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cluster),
+      "r"(src), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
+}  // namespace dcp
+
+namespace dcp {
+
+// arrive.expect_tx without release semantics: for arming a barrier for the
+// next transfer, which publishes nothing of this thread's.
+__device__ __forceinline__ void mbar_arrive_expect_tx_relaxed(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+}  // namespace dcp
+
+namespace dcp {
+
+// Bounded wait for two phases at once (acquire at cluster scope).  Both
+// polls are issued back to back, so waiting on phases that have already
+// completed costs one round trip rather than two.
+__device__ __forceinline__ bool mbar_wait2_cluster(uint32_t a, uint32_t pa, uint32_t b,
+                                                   uint32_t pb) {
+  bool da = false, db = false;
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (!da) da = mbar_try_wait_cluster(a, pa);
+    if (!db) db = mbar_try_wait_cluster(b, pb);
+    if (da && db) return true;
+  }
+  return false;
+}
+
+}  // namespace dcp
