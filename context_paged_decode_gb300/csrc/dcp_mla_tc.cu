@@ -89,8 +89,9 @@ constexpr int kRopeTileBytes = kSt * 64;               // 4 KB: 64 tokens x 32 r
 constexpr int kStageBytes = 4 * kChunkBytes + kRopeTileBytes;  // 36 KB
 constexpr int kXsPlane = kOwn * 128;                   // 8 KB: 32 fp32 columns of the own rows
 constexpr int kXsBytes = 2 * kXsPlane;                 // 16 KB of the peer's partial scores
-constexpr int kPtBytes = kHeads * 128;                 // 16 KB: P, 128 rows x 64 bf16
-constexpr int kSideBytes = kOwn * 16;                  // (factor, sum of each half, 0) per own row
+constexpr int kPtBlock = kHeads * 64;                  // 8 KB: P for 32 tokens, 64-byte rows
+constexpr int kPtBytes = 2 * kPtBlock;                 // 16 KB: P, 128 rows x 64 bf16
+constexpr int kSideBytes = 2 * kOwn * 8;               // (factor, half-row sum) per half and own row
 constexpr int kPMsgBytes = kOwn * 128 + kSideBytes;    // what the peer's softmax sends per stage
 constexpr int kQRopeBytes = kHeads * 64;               // 8 KB: this CTA's rope half of Q
 constexpr int kKvOff = 0;
@@ -101,8 +102,8 @@ constexpr int kQRopeOff = kPtOff + 2 * kPtBytes;       // 208 KB
 constexpr int kSideOwnOff = kQRopeOff + kQRopeBytes;   // 216 KB
 constexpr int kSideRecvOff = kSideOwnOff + 2 * kSideBytes;
 constexpr int kMxOff = kSideRecvOff + 2 * kSideBytes;  // half-row maxima, [sb][half][row]
-constexpr int kBarOff = kMxOff + 2 * 2 * kOwn * 4;      // 221 KB
-constexpr int kNumBars = 30;
+constexpr int kBarOff = kMxOff + 3 * 2 * kOwn * 4;      // 221.5 KB
+constexpr int kNumBars = 28;
 constexpr int kMlaSmem = 1024 + kBarOff + kNumBars * 8 + 16;
 constexpr int kFirstRowWarp = 3;
 constexpr int kMlaThreads = 32 * (kFirstRowWarp + 8);  // 352
@@ -139,17 +140,18 @@ enum : int {
   B_Q_EMPTY = 23,
   B_O_FULL = 24,
   B_O_FREE = 25,
-  B_MX = 26,        // +own quarter: both halves of its rows stored their maxima (per stage)
-  B_PQ = 28         // +own quarter: both halves of its rows stored P (per stage)
+  B_MX = 26         // +own quarter: both halves of its rows stored their maxima (per stage,
+                    // plus one phase per item for the row sums)
 };
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kSt, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kDvHalf, false, true);
 
 __device__ __forceinline__ int arrivals(int i) {
-  if (i == B_S_FREE || i == B_S_FREE + 1 || i == B_O_FREE) return 6;
-  if (i == B_P_FULL || i == B_P_FULL + 1 || i == B_Q_FULL || i == B_XS_FREE) return 4;
-  if (i == B_PT_FREE || i == B_PT_FREE + 1 || (i >= B_MX && i < B_MX + 4)) return 2;
+  if (i == B_S_FREE || i == B_S_FREE + 1 || i == B_O_FREE || i == B_P_FULL || i == B_P_FULL + 1)
+    return 6;
+  if (i == B_Q_FULL || i == B_XS_FREE) return 4;
+  if (i == B_PT_FREE || i == B_PT_FREE + 1 || i == B_MX || i == B_MX + 1) return 2;
   return 1;
 }
 
@@ -337,14 +339,16 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           tc_fence_after();
           // V = this CTA's four value chunks, the MN-major B operand: 64-column
           // atoms kChunkBytes apart, 8-token groups 1024 B apart; k-step kk
-          // starts 16 tokens further.  P (K-major A operand) is P tile sb.
+          // starts 16 tokens further.  P (K-major A operand) is P tile sb: two
+          // 32-token blocks of 64-byte rows (64-byte swizzle, 8-row groups
+          // 512 B apart), so k-step kk reads block kk / 2 at byte 32 (kk % 2).
           const uint32_t v = sbase + kKvOff + st * kStageBytes;
-          const uint64_t p_a = sdesc_sw128(sbase + kPtOff + sb * kPtBytes, 0, 1024);
+          const uint32_t pt = sbase + kPtOff + sb * kPtBytes;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = sdesc_sw128(v + kk * 16 * 128, kChunkBytes, 1024);
-            tc_mma_ss(tmem + kColO, p_a + (uint64_t)((kk * 32) >> 4), bd, kIdescPV,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t pa = sdesc_sw64(pt + (kk >> 1) * kPtBlock + (kk & 1) * 32, 512);
+            tc_mma_ss(tmem + kColO, pa, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(bars + 8 * (B_KV_EMPTY + st));
           // P tile sb of both CTAs may be rewritten once both P V have read it
@@ -514,7 +518,7 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
       if (dead && lane == 0) atomicAdd(errp, kStuckMla);
     } else if (role == 2) {
       // ---------- receiver: the peer's P rows for its heads ----------
-      const uint32_t side = sbase + kSideRecvOff + hp * 16;
+      const uint32_t side = sbase + kSideRecvOff + hp * 8;
       const bool armer = lane == 0 && (q4 & 1) == 0;
       uint32_t g = 0, k = 0;
       bool dead = false;
@@ -531,13 +535,13 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
             dead = true;
             break;
           }
-          // side entry: (f, l of half 0, l of half 1, -)
+          // side entries: (f, half-row sum) of half 0 and of half 1
           float f, l0, l1;
           asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];"
                        : "=f"(f), "=f"(l0)
                        : "r"(side + sb * kSideBytes));
-          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l1) : "r"(side + sb * kSideBytes + 8));
-          lr = l0 + l1;
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l1) : "r"(side + sb * kSideBytes + kOwn * 8 + 4));
+          lr = l0 + l1;   // both halves carry the same factor
           // the tile's next phase (stage gj + 2) expects the peer's bytes again
           if (armer) mbar_arrive_expect_tx_relaxed(bars + 8 * (B_P_RECV + sb), kPMsgBytes);
           if (__any_sync(0xffffffffu, f != 1.f)) {
@@ -571,19 +575,36 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
       const int stid = h * 64 + qo * 32 + lane;      // 0..127
       const bool lead = lane == 0;
       const bool armer = lead && h == 0 && qo == 0;
-      const uint32_t xrow = sbase + kXsOff + h * kXsPlane + hp * 128;  // my half-row of the slots
-      const uint32_t prow = sbase + kPtOff + head * 128;               // my row of the P tiles
-      const uint32_t side = sbase + kSideOwnOff + hp * 16;
+      const uint32_t xrow = sbase + kXsOff + h * kXsPlane + hp * 128;  // my half-row of the slot
+      // my row of P block h (64-byte rows, 16-byte units swizzled by (row >> 1) & 3)
+      const uint32_t prow = sbase + kPtOff + h * kPtBlock + head * 64;
+      const uint32_t pswz = (uint32_t)((head >> 1) & 3);
+      const uint32_t side = sbase + kSideOwnOff + (h * kOwn + hp) * 8;
+      // half-row maxima: slots [stage parity][half][row]; slot 2 carries the row sums
       const uint32_t mx_mine = sbase + kMxOff + (h * kOwn + hp) * 4;
       const uint32_t mx_other = sbase + kMxOff + ((1 - h) * kOwn + hp) * 4;
-      const uint32_t mxbar = bars + 8 * (B_MX + qo), pqbar = bars + 8 * (B_PQ + qo);
+      const uint32_t mxbar = bars + 8 * (B_MX + qo);
       const uint32_t xsfree_peer = mapa_shared(bars + 8 * B_XS_FREE, peer);
       const uint32_t precv_peer = mapa_shared(bars + 8 * B_P_RECV, peer);
-      const uint32_t pt_peer = mapa_shared(sbase + kPtOff + q4 * 4096, peer);
-      const uint32_t side_peer = mapa_shared(sbase + kSideRecvOff + qo * 512, peer);
-      uint32_t g = 0, k = 0, qv = 0;
+      // this warp's 32 rows of P block h and its 32 side entries, in the peer
+      const uint32_t pt_peer = mapa_shared(sbase + kPtOff + h * kPtBlock + q4 * 2048, peer);
+      const uint32_t side_peer = mapa_shared(sbase + kSideRecvOff + (h * kOwn + qo * 32) * 8, peer);
+      uint32_t g = 0, k = 0, qv = 0, mxc = 0;
       int prev_b = -1;
       bool dead = false;
+      // bf16 P of my half-row relative to the maximum mb, and its sum
+      auto make_p = [&](const float (&sc)[32], int nv, float mb, uint32_t (&pk)[16]) -> float {
+        float ls = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int i = 2 * e;
+          const float pa = i < nv ? ex2_ftz(fmaf(sc[i], A.sl2, -mb)) : 0.f;
+          const float pq = i + 1 < nv ? ex2_ftz(fmaf(sc[i + 1], A.sl2, -mb)) : 0.f;
+          ls += pa + pq;
+          pk[e] = pack_bf16(pa, pq);
+        }
+        return ls;
+      };
       for (int it = i0; it < i1 && !dead; ++it, ++k) {
         const int4 d = plan.item[it];
         const int b = d.x, r = d.y & 255, p0 = d.z, p1 = d.w;
@@ -601,10 +622,8 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
         int32_t ph[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) ph[i] = i < nst ? bt_raw(b, r, p0, i) : -1;
-        uint32_t sb_last = 0;
         for (int j = 0; j < nst; ++j) {
           const uint32_t gj = g + j, sb = gj & 1, us = gj >> 1;
-          sb_last = sb;
           const int32_t phj = ph[0];
           ph[0] = ph[1];
           ph[1] = ph[2];
@@ -613,7 +632,7 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           const int nvalid = usable(phj) ? min(kSt, p1 - (p0 + j * kSt)) : 0;
           const int nv = nvalid - 32 * h;            // valid columns of my half (may be <= 0)
           // full scores of my half of stage gj: this CTA's partial (tensor
-          // memory) plus the peer's (receive slot sb), 32 columns
+          // memory) plus the peer's (receive slot), 32 columns
           if (!cwait2(bars + 8 * (B_S_FULL + sb), us & 1, bars + 8 * B_X_FULL, gj & 1)) {
             dead = true;
             break;
@@ -626,14 +645,13 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
             tc_wait_ld(s0);
             tc_fence_before();
             warp_arrive(bars + 8 * (B_S_FREE + sb));
-            const uint32_t src = xrow;
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
               const uint32_t pu = (uint32_t)((t ^ (hp & 7)) << 4);
               uint32_t a0, a1, a2, a3;
               asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                            : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                           : "r"(src + pu));
+                           : "r"(xrow + pu));
               sc[4 * t + 0] = __uint_as_float(s0[4 * t + 0]) + __uint_as_float(a0);
               sc[4 * t + 1] = __uint_as_float(s0[4 * t + 1]) + __uint_as_float(a1);
               sc[4 * t + 2] = __uint_as_float(s0[4 * t + 2]) + __uint_as_float(a2);
@@ -666,10 +684,11 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
                        : "memory");
           warp_arrive(mxbar);
           // also P tile sb: free once the P V of stage gj - 2 completed in both CTAs
-          if (!cwait2(mxbar, gj & 1, bars + 8 * (B_PT_FREE + sb), (us & 1) ^ 1)) {
+          if (!cwait2(mxbar, mxc & 1, bars + 8 * (B_PT_FREE + sb), (us & 1) ^ 1)) {
             dead = true;
             break;
           }
+          ++mxc;
           float mo;
           asm volatile("ld.shared.f32 %0, [%1];" : "=f"(mo) : "r"(mx_other + sb * (2 * kOwn * 4)));
           const float mx = fmaxf(t16[0], mo) * A.sl2;
@@ -688,33 +707,18 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
             rescale_o(f, h * (kDvHalf / 2), kDvHalf / 64);
           }
           if (grow) m = mx;
-          const float mb = (m == -INFINITY) ? 0.f : m;
-          // my half of P row `head` (32 tokens, bf16)
           uint32_t pk[16];
-          float ls = 0.f;
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int i = 2 * e;
-            const float pa = i < nv ? ex2_ftz(fmaf(sc[i], A.sl2, -mb)) : 0.f;
-            const float pq = i + 1 < nv ? ex2_ftz(fmaf(sc[i + 1], A.sl2, -mb)) : 0.f;
-            ls += pa + pq;
-            pk[e] = pack_bf16(pa, pq);
-          }
+          const float ls = make_p(sc, nv, (m == -INFINITY) ? 0.f : m, pk);
           lh = lh * f + ls;
           const uint32_t pr = prow + sb * kPtBytes;
 #pragma unroll
           for (int t = 0; t < 4; ++t)
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
-                             pr + (((4 * h + t) ^ (head & 7)) << 4)),
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(pr + ((t ^ pswz) << 4)),
                          "r"(pk[4 * t]), "r"(pk[4 * t + 1]), "r"(pk[4 * t + 2]), "r"(pk[4 * t + 3])
                          : "memory");
-          if (h == 0)
-            asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(side + sb * kSideBytes), "f"(f),
-                         "f"(lh)
-                         : "memory");
-          else
-            asm volatile("st.shared.f32 [%0], %1;" ::"r"(side + sb * kSideBytes + 8), "f"(lh)
-                         : "memory");
+          asm volatile("st.shared.v2.f32 [%0], {%1,%2};" ::"r"(side + sb * kSideBytes), "f"(f),
+                       "f"(lh)
+                       : "memory");
           if (nvalid < kSt) {
             // rows past the end may hold anything: zero this CTA's V columns so 0 * x stays 0
             const uint32_t st = gj % kNs;
@@ -733,36 +737,34 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
             }
           }
           fence_proxy_async_smem();   // P, the side values and zeroed V rows are read asynchronously
-          warp_arrive(pqbar);
-          if (!wwait(pqbar, gj & 1)) {
-            dead = true;
-            break;
-          }
-          if (h == 0 && lead) {
-            // these 32 P rows and side entries -> the same places in the peer
-            bulk_copy_cluster(pt_peer + sb * kPtBytes, sbase + kPtOff + sb * kPtBytes + q4 * 4096,
-                              4096, precv_peer + 8 * sb);
+          __syncwarp();
+          if (lead) {
+            // my 32 rows of P block h and my side entries -> the same places in the peer
+            bulk_copy_cluster(pt_peer + sb * kPtBytes,
+                              sbase + kPtOff + sb * kPtBytes + h * kPtBlock + q4 * 2048, 2048,
+                              precv_peer + 8 * sb);
             bulk_copy_cluster(side_peer + sb * kSideBytes,
-                              sbase + kSideOwnOff + sb * kSideBytes + qo * 512, 512,
+                              sbase + kSideOwnOff + sb * kSideBytes + (h * kOwn + qo * 32) * 8, 256,
                               precv_peer + 8 * sb);
             mbar_arrive(bars + 8 * (B_P_FULL + sb));
           }
         }
         if (dead) break;
         g += nst;
+        // the row sum: exchange the half-row sums through slot 2
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(mx_mine + 2 * (2 * kOwn * 4)), "f"(lh)
+                     : "memory");
+        warp_arrive(mxbar);
         // epilogue: my half of O / l -> item partial, LSE in natural log
-        if (!wwait(bars + 8 * B_O_FULL, k & 1)) {
+        if (!wwait(mxbar, mxc & 1) || !wwait(bars + 8 * B_O_FULL, k & 1)) {
           dead = true;
           break;
         }
+        ++mxc;
+        float lo;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(lo) : "r"(mx_other + 2 * (2 * kOwn * 4)));
+        const float l = h == 0 ? lh + lo : lo + lh;  // (half 0) + (half 1), as the peer adds them
         tc_fence_after();
-        // side entry of the last stage: (f, l of half 0, l of half 1, -)
-        float l0 = 0.f, l1 = 0.f;
-        if (nst > 0) {
-          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l0) : "r"(side + sb_last * kSideBytes + 4));
-          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l1) : "r"(side + sb_last * kSideBytes + 8));
-        }
-        const float l = l0 + l1;
         write_o(it, l, h * (kDvHalf / 2), kDvHalf / 64);
         if (h == 0)
           plan.lse[(int64_t)it * kHeads + head] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
