@@ -47,19 +47,22 @@ struct ItemParts {  // plan items: lse [item][G], o [item][G][dv]
   }
 };
 
-// One warp per output row.  Lane i computes the weight of part i (in blocks of
-// 32 parts) once; the weights are broadcast with shuffles while every lane
-// accumulates CH float4 columns, four parts per iteration so several loads
-// are in flight.
+// One warp per output row.  With at most 32 parts, lane i holds part i's
+// LSE, so the maximum, the sum and every part's weight come from one round
+// of loads and warp shuffles; the partial rows are then read four parts at
+// a time, all loads of a group issued before any is used.  More parts take
+// the same steps in blocks of 32.
 template <int CH, class Parts>
 __device__ __forceinline__ void merge_row(const Parts& P, int n, int64_t row, int dv,
                                           bool has_sink, float sink, void* out, int out_dtype,
                                           int64_t out_row, float* out_lse) {
   const int lane = threadIdx.x & 31;
-  float m = has_sink ? sink : -INFINITY;
-  for (int i = lane; i < n; i += 32) m = fmaxf(m, P.lse_at(i, row));
-  m = warp_max(m);
   const int nv = dv >> 2;
+  const float l_mine = lane < n ? P.lse_at(lane, row) : -INFINITY;
+  float m = has_sink ? sink : -INFINITY;
+  m = fmaxf(m, l_mine);
+  for (int i = 32 + lane; i < n; i += 32) m = fmaxf(m, P.lse_at(i, row));
+  m = warp_max(m);
   if (m == -INFINITY) {  // nothing attended and no sink
     for (int c = lane; c < nv; c += 32) {
       if (out_dtype == DCP_F32)
@@ -70,8 +73,8 @@ __device__ __forceinline__ void merge_row(const Parts& P, int n, int64_t row, in
     if (out_lse && lane == 0) out_lse[out_row] = -INFINITY;
     return;
   }
-  float s = 0.f;
-  for (int i = lane; i < n; i += 32) {
+  float s = l_mine != -INFINITY ? expf(l_mine - m) : 0.f;
+  for (int i = 32 + lane; i < n; i += 32) {
     const float l = P.lse_at(i, row);
     if (l != -INFINITY) s += expf(l - m);
   }
@@ -84,24 +87,33 @@ __device__ __forceinline__ void merge_row(const Parts& P, int n, int64_t row, in
   for (int blk = 0; blk < n; blk += 32) {
     float wl = 0.f;
     if (blk + lane < n) {
-      const float l = P.lse_at(blk + lane, row);
+      const float l = blk == 0 ? l_mine : P.lse_at(blk + lane, row);
       wl = l == -INFINITY ? 0.f : expf(l - lse);
     }
     const int cnt = min(32, n - blk);
-#pragma unroll 4
-    for (int ii = 0; ii < cnt; ++ii) {
-      const float w = __shfl_sync(0xffffffffu, wl, ii);
-      const float4* src = reinterpret_cast<const float4*>(P.o_at(blk + ii, row, dv));
+    for (int i0 = 0; i0 < cnt; i0 += 4) {
+      // up to four parts: every load first, then the weighted sums in part order
+      float4 v[4][CH];
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        const int idx = lane + 32 * c;
-        if (idx < nv) {
-          const float4 v = __ldg(src + idx);
-          if (w != 0.f) {  // an empty part adds nothing, whatever its o holds
-            acc[c].x = fmaf(w, v.x, acc[c].x);
-            acc[c].y = fmaf(w, v.y, acc[c].y);
-            acc[c].z = fmaf(w, v.z, acc[c].z);
-            acc[c].w = fmaf(w, v.w, acc[c].w);
+      for (int q = 0; q < 4; ++q) {
+        const float4* src =
+            reinterpret_cast<const float4*>(P.o_at(blk + min(i0 + q, cnt - 1), row, dv));
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int idx = lane + 32 * c;
+          v[q][c] = (i0 + q < cnt && idx < nv) ? __ldg(src + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float w = __shfl_sync(0xffffffffu, wl, min(i0 + q, 31));
+        if (i0 + q < cnt && w != 0.f) {  // an empty part adds nothing, whatever its o holds
+#pragma unroll
+          for (int c = 0; c < CH; ++c) {
+            acc[c].x = fmaf(w, v[q][c].x, acc[c].x);
+            acc[c].y = fmaf(w, v[q][c].y, acc[c].y);
+            acc[c].z = fmaf(w, v[q][c].z, acc[c].z);
+            acc[c].w = fmaf(w, v[q][c].w, acc[c].w);
           }
         }
       }
