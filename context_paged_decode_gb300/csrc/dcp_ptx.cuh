@@ -194,25 +194,6 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
-// 32 lanes x 16 consecutive 32-bit columns.
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tc_wait_ld16(uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.wait::ld.sync.aligned;"
-      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
-        "+r"(r[14]), "+r"(r[15])
-      :
-      : "memory");
-}
 // Wait for outstanding tcgen05.ld; the registers are threaded through so no
 // use of them can be scheduled before the wait.
 __device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[32]) {
@@ -224,20 +205,6 @@ __device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[32]) {
         "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
         "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
       :
-      : "memory");
-}
-__device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-      : "memory");
-}
-__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -270,17 +237,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                              uint32_t d) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b),
-               "r"(c), "r"(d)
-               : "memory");
-}
-// Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -296,16 +252,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity)
   for (uint32_t i = 0; i < kWaitLimit; ++i)
     if (mbar_try_wait_cluster(bar, parity)) return true;
   return false;
-}
-// Asynchronous 16-byte store into another CTA's shared memory that completes
-// 16 transaction bytes on that CTA's mbarrier (no fence on the sender).
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b,
-                                            uint32_t c, uint32_t d, uint32_t cluster_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(
-          cluster_addr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
-      : "memory");
 }
 // 2^x with subnormal results flushed to zero (ex2.approx.ftz).
 __device__ __forceinline__ float ex2_ftz(float x) {
@@ -334,18 +280,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-}  // namespace dcp
 
-namespace dcp {
-
-// Named barrier over `count` threads (id 1..15; 0 is __syncthreads).
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-}  // namespace dcp
-
-namespace dcp {
 
 // Arrive on a barrier of another CTA of the cluster without release
 // semantics.  `dep` is a value computed from every shared-memory load the
@@ -374,9 +309,7 @@ __device__ __forceinline__ bool mbar_wait_relaxed_cluster(uint32_t bar, uint32_t
   return false;
 }
 
-}  // namespace dcp
 
-namespace dcp {
 
 // Prefetch one tile of a tensor map into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t x, int32_t y) {
@@ -385,9 +318,7 @@ __device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t x, int
                : "memory");
 }
 
-}  // namespace dcp
 
-namespace dcp {
 
 // Shared-memory matrix descriptor, 64-byte swizzle (rows of 64 bytes, 8-row
 // groups `sbo` apart): layout type 4 at [61,64).
@@ -406,9 +337,7 @@ __device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t cta_m
       : "memory");
 }
 
-}  // namespace dcp
 
-namespace dcp {
 
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
 // from this CTA's shared memory into another CTA's of the cluster; the bytes
@@ -422,9 +351,7 @@ __device__ __forceinline__ void bulk_copy_cluster(uint32_t dst_cluster, uint32_t
       : "memory");
 }
 
-}  // namespace dcp
 
-namespace dcp {
 
 // arrive.expect_tx without release semantics: for arming a barrier for the
 // next transfer, which publishes nothing of this thread's.
@@ -434,9 +361,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_relaxed(uint32_t bar, uint
                : "memory");
 }
 
-}  // namespace dcp
 
-namespace dcp {
 
 // Bounded wait for two phases at once (acquire at cluster scope).  Both
 // polls are issued back to back, so waiting on phases that have already
