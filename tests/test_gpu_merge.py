@@ -11,7 +11,9 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("n,B,H,dv", [(1, 1, 1, 4), (2, 3, 8, 64), (8, 32, 32, 128),
-                                      (8, 4, 128, 512), (13, 2, 5, 1024)])
+                                      (8, 4, 128, 512), (13, 2, 5, 1024),
+                                      # more parts than a warp has lanes: LSEs in blocks of 32
+                                      (33, 2, 4, 128), (70, 1, 3, 512)])
 @pytest.mark.parametrize("with_sink", [False, True])
 def test_merge_matches_oracle(lib, n, B, H, dv, with_sink):
     rng = np.random.default_rng(n * 31 + dv)

@@ -123,6 +123,29 @@ def mla_sampled(lib, cfg, reqs, heads_per_req, seed):
                 ref.check_bf16(po[r, b, h], pl[r, b, h], po_ref[r], pl_ref[r], f"r{r} b{b} h{h}")
 
 
+def test_mla_bad_block_table_entries_are_counted(lib):
+    """Unusable block-table entries are counted, their stages attend nothing,
+    and requests that do not touch them still match the oracle."""
+    cfg = dataclasses.replace(MLA, B=2, lengths=[700, 300], dcp=2, bs=64, I=1)
+    wl = D.build(cfg)
+    bt = wl.block_table.clone()
+    bt[1, 0, 2] = wl.num_blocks + 5     # rank 1, request 0, virtual block 2
+    bt[0, 0, 1] = -3                    # rank 0, request 0, virtual block 1
+    import context_paged_decode_gb300 as dcp
+    kv = dcp.PagedKV(wl.k_pools, None, bt, wl.num_blocks)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = lib.decode_mla(wl.layout, wl.q, kv, wl.local_lens, cfg.scale, cfg.dv,
+                              out_dtype=torch.float32, err=err)
+    torch.cuda.synchronize()
+    assert 0 < err.item() < (1 << 20)   # counted; no wait timed out
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    heads = [0, 77, 127]
+    exp = ref.mla_expected(cfg, wl.seq_lens_host, 1, heads)
+    for h in heads:
+        check(cfg, out[1, h], lse[1, h], exp[h][0], exp[h][1], f"b1 h{h}")
+
+
 def test_mla_bf16_b64_full_size_sampled(lib):
     lens = W.make_seq_lens(MLA)
     order = np.argsort(lens)
