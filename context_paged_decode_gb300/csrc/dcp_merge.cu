@@ -133,6 +133,112 @@ __device__ __forceinline__ void merge_row(const Parts& P, int n, int64_t row, in
   if (out_lse && lane == 0) out_lse[out_row] = lse;
 }
 
+// The same merge with one CTA of kWideWarps warps per output row, for calls
+// with too few rows to fill the GPU one warp per row (a long request split
+// into hundreds of parts).  Warp w takes parts [n w / W, n (w+1) / W); the
+// warps' maxima, sums and weighted partial rows are combined in shared
+// memory in warp order, so the result does not depend on timing.
+constexpr int kWideWarps = 8;
+
+template <int CH, class Parts>
+__device__ __forceinline__ void merge_row_wide(const Parts& P, int n, int64_t row, int dv,
+                                               bool has_sink, float sink, void* out,
+                                               int out_dtype, int64_t out_row, float* out_lse) {
+  extern __shared__ float4 wide_acc[];               // [kWideWarps][nv]
+  __shared__ float wm[kWideWarps], ws[kWideWarps];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int nv = dv >> 2;
+  const int p0 = (int)((int64_t)n * w / kWideWarps), p1 = (int)((int64_t)n * (w + 1) / kWideWarps);
+  float m = -INFINITY;
+  for (int i = p0 + lane; i < p1; i += 32) m = fmaxf(m, P.lse_at(i, row));
+  m = warp_max(m);
+  if (lane == 0) wm[w] = m;
+  __syncthreads();
+  m = has_sink ? sink : -INFINITY;
+  for (int i = 0; i < kWideWarps; ++i) m = fmaxf(m, wm[i]);
+  if (m == -INFINITY) {  // nothing attended and no sink
+    for (int c = threadIdx.x; c < nv; c += blockDim.x) {
+      if (out_dtype == DCP_F32)
+        reinterpret_cast<float4*>(out)[out_row * nv + c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      else
+        reinterpret_cast<uint2*>(out)[out_row * nv + c] = make_uint2(0u, 0u);
+    }
+    if (out_lse && threadIdx.x == 0) out_lse[out_row] = -INFINITY;
+    return;
+  }
+  float s = 0.f;
+  for (int i = p0 + lane; i < p1; i += 32) {
+    const float l = P.lse_at(i, row);
+    if (l != -INFINITY) s += expf(l - m);
+  }
+  s = warp_sum(s);
+  if (lane == 0) ws[w] = s;
+  __syncthreads();
+  s = 0.f;
+  for (int i = 0; i < kWideWarps; ++i) s += ws[i];
+  if (has_sink) s += expf(sink - m);
+  const float lse = m + logf(s);
+  float4 acc[CH];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int blk = p0; blk < p1; blk += 32) {
+    float wl = 0.f;
+    if (blk + lane < p1) {
+      const float l = P.lse_at(blk + lane, row);
+      wl = l == -INFINITY ? 0.f : expf(l - lse);
+    }
+    const int cnt = min(32, p1 - blk);
+    for (int i0 = 0; i0 < cnt; i0 += 4) {
+      float4 v[4][CH];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4* src =
+            reinterpret_cast<const float4*>(P.o_at(blk + min(i0 + q, cnt - 1), row, dv));
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int idx = lane + 32 * c;
+          v[q][c] = (i0 + q < cnt && idx < nv) ? __ldg(src + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float wt = __shfl_sync(0xffffffffu, wl, min(i0 + q, 31));
+        if (i0 + q < cnt && wt != 0.f) {
+#pragma unroll
+          for (int c = 0; c < CH; ++c) {
+            acc[c].x = fmaf(wt, v[q][c].x, acc[c].x);
+            acc[c].y = fmaf(wt, v[q][c].y, acc[c].y);
+            acc[c].z = fmaf(wt, v[q][c].z, acc[c].z);
+            acc[c].w = fmaf(wt, v[q][c].w, acc[c].w);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int idx = lane + 32 * c;
+    if (idx < nv) wide_acc[w * nv + idx] = acc[c];
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < nv; c += blockDim.x) {
+    float4 t = wide_acc[c];
+    for (int i = 1; i < kWideWarps; ++i) {
+      const float4 u = wide_acc[i * nv + c];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+    }
+    if (out_dtype == DCP_F32)
+      reinterpret_cast<float4*>(out)[out_row * nv + c] = t;
+    else
+      reinterpret_cast<uint2*>(out)[out_row * nv + c] =
+          make_uint2(pack_bf16(t.x, t.y), pack_bf16(t.z, t.w));
+  }
+  if (out_lse && threadIdx.x == 0) out_lse[out_row] = lse;
+}
+
 template <int CH>
 __global__ void dense_merge_kernel(int n, const float* __restrict__ po,
                                    const float* __restrict__ pl, int B, int H, int dv,
@@ -183,14 +289,50 @@ __global__ void item_merge_kernel(Plan plan, int mode, int B, int dcp, int Hq, i
             mode == 0 ? out_dtype : (int)DCP_F32, row, out_lse);
 }
 
+// item_merge_kernel with one CTA per output row (merge_row_wide).
+template <int CH>
+__global__ void __launch_bounds__(kWideWarps * 32)
+item_merge_wide_kernel(Plan plan, int mode, int B, int dcp, int Hq, int G, int groups, int dv,
+                       const float* __restrict__ sink, void* out, int out_dtype, float* out_lse) {
+  const int64_t row = blockIdx.x;
+  const int h = (int)(row % Hq);
+  const int b = (int)((row / Hq) % B);
+  const int r = mode == 0 ? 0 : (int)(row / ((int64_t)B * Hq));
+  const int g = h / G, hh = h % G;
+  const int e = (b * groups + g) * dcp;
+  const int first = plan.off[e + r];
+  const int last = plan.off[e + (mode == 0 ? dcp : r + 1)];
+  ItemParts P{plan.o, plan.lse, first, G, hh};
+  const bool hs = (mode == 0) && sink != nullptr;
+  merge_row_wide<CH>(P, last - first, row, dv, hs, hs ? sink[h] : 0.f, out,
+                     mode == 0 ? out_dtype : (int)DCP_F32, row, out_lse);
+}
+
 int launch_item_merge(const Plan& plan, int mode, int B, int dcp, int Hq, int G, int groups,
                       int dv, const float* sink, void* out, int out_dtype, float* out_lse,
                       cudaStream_t s) {
   const int64_t rows = (int64_t)(mode == 0 ? 1 : dcp) * B * Hq;
   if (rows == 0) return DCP_OK;
+  const int nv = dv / 4;
+  if (rows < 4 * (int64_t)num_sms()) {
+    // few rows (few, long requests): one CTA of kWideWarps warps per row
+    const size_t smem = (size_t)kWideWarps * nv * sizeof(float4);
+#define DCP_ITEM_WIDE(CH)                                                                      \
+  item_merge_wide_kernel<CH><<<(unsigned)rows, kWideWarps * 32, smem, s>>>(                    \
+      plan, mode, B, dcp, Hq, G, groups, dv, sink, out, out_dtype, out_lse)
+    if (nv <= 32)
+      DCP_ITEM_WIDE(1);
+    else if (nv <= 64)
+      DCP_ITEM_WIDE(2);
+    else if (nv <= 128)
+      DCP_ITEM_WIDE(4);
+    else
+      DCP_ITEM_WIDE(8);
+#undef DCP_ITEM_WIDE
+    return launch_status();
+  }
   const int wpb = 8;
   const unsigned grid = (unsigned)((rows + wpb - 1) / wpb);
-  const int nv = dv / 4;
   if (nv <= 32)
     item_merge_kernel<1><<<grid, wpb * 32, 0, s>>>(plan, mode, B, dcp, Hq, G, groups, dv, sink,
                                                    out, out_dtype, out_lse);
