@@ -10,12 +10,14 @@ bimodal 1k-256k contexts, dcp=8, block_size 16 (other workloads with
 --config).  The KV cache is resident state, built once before timing.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--config NAME] [--no-cpu-baseline]
+                  [--config NAME] [--no-cpu-baseline] [--no-graph]
 
 Prints one JSON line (rank 0).  ``value`` is KV-read GB/s of the step
-(KV bytes the step must read / device time), ``e2e`` the same metric with
-the per-step inputs copied from pinned host memory and the output copied
-back inside the timed region.
+(KV bytes the step must read / device time).  The timed steps replay the
+step captured once as a CUDA graph, as a serving loop would (``--no-graph``
+launches the kernels one by one).  ``e2e`` is the same metric through eager
+calls, with the per-step inputs copied from pinned host memory and the
+output copied back inside the timed region.
 """
 from __future__ import annotations
 
@@ -26,6 +28,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -98,17 +101,37 @@ def step_flops(cfg, lens, B):
 
 
 class Clocks:
-    """nvidia-smi samples during the timed region."""
+    """nvidia-smi samples (every 100 ms) around the timed region.
+
+    Samples taken inside [begin, end] are used; a region shorter than the
+    sampling interval is represented by the last sample before it and the
+    first after it ("bracketing")."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.samples = []          # (time, sm, max, reasons)
+        self.t0 = self.t1 = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm, mx = float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            rs = {n for n, v in zip(self.NAMES, f[5:9]) if v.lower().startswith("active")}
+            self.samples.append((time.monotonic(), sm, mx, rs))
 
     def start(self):
+        """Start sampling and wait (up to 3 s) for the first sample."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
@@ -116,33 +139,40 @@ class Clocks:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
+        threading.Thread(target=self._reader, daemon=True).start()
+        t_end = time.monotonic() + 3.0
+        while not self.samples and time.monotonic() < t_end:
+            time.sleep(0.01)
+
+    def begin(self):
+        self.t0 = time.monotonic()
+
+    def end(self):
+        self.t1 = time.monotonic()
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        t_end = time.monotonic() + 1.0  # one sample after the region
+        while time.monotonic() < t_end and not (self.samples and self.samples[-1][0] > self.t1):
+            time.sleep(0.01)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.communicate(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
+        inside = [x for x in self.samples if self.t0 <= x[0] <= self.t1]
+        how = "inside the timed region"
+        if not inside:
+            before = [x for x in self.samples if x[0] < self.t0][-1:]
+            after = [x for x in self.samples if x[0] > self.t1][:1]
+            inside, how = before + after, "bracketing the timed region (shorter than the 100 ms interval)"
+        sm = [x[1] for x in inside]
+        reasons = set().union(*[x[3] for x in inside]) if inside else set()
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "sm_max_mhz": max(x[2] for x in inside) if inside else None,
+                "reasons": sorted(reasons), "samples": len(inside), "sampled": how}
 
 
 # ---------------------------------------------------------------------------
@@ -282,16 +312,28 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    run_step = step
+    if not args.no_graph:
+        # the step as one CUDA graph: every call reads its sizes from device
+        # memory and allocates nothing, so the launches capture as they are
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        run_step = graph.replay
 
     # timed steps (device time, CUDA events on the launching stream)
     clk = Clocks(local_rank)
     clk.start()
     barrier()
     torch.cuda.synchronize()
+    clk.begin()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        run_step()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -306,6 +348,7 @@ def run_ours(args, rank, world, local_rank):
         b.record(stream)
         b.synchronize()
         dec_ms.append(a.elapsed_time(b))
+    clk.end()
     clocks = clk.stop()
 
     # end to end: host inputs (pinned) -> device, step, output -> host
@@ -379,7 +422,9 @@ def run_ours(args, rank, world, local_rank):
                    "kv_bytes_per_step": kv_bytes, "l2": "inputs larger than L2 (KV >> 129 MB)"
                    if kv_bytes > 512 << 20 else "working set fits L2; not flushed",
                    "parallelism": f"dcp{cfg.dcp} virtual ranks on 1 GPU" +
-                                  (f" x {world} replicas" if world > 1 else "")},
+                                  (f" x {world} replicas" if world > 1 else ""),
+                   "launch": "step kernels launched one by one" if args.no_graph
+                             else "step replayed as one CUDA graph (e2e: eager calls)"},
         "decode_tok_per_s": round(job_value(B, world, step_ms * 1e-3), 1),
         "e2e": {"value": round(job_value(kv_bytes, world, e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
@@ -486,6 +531,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="gqa_bf16_b32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the step's kernels one by one instead of replaying a CUDA graph")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--reqs", type=int, default=0,
                     help="keep only the first N requests of the workload (profiling cases)")
