@@ -36,8 +36,9 @@
 //    (each is refilled once the peer has read the previous stage, early in
 //    its softmax), two 16 KB P tiles (128 rows x 64 bf16, the A operand of
 //    P V), the (factor, sum) side arrays and the rope half of Q;
-//  * warps: 0 issues TMA (the tiles three stages beyond the ring are
-//    prefetched into L2), 1 issues Q K^T, 2 issues P V.  Warps 3-10 each sit
+//  * warps: 0 issues TMA (no separate L2 prefetch: with the 4-deep ring it
+//    only added traffic and issue time, 1.92 -> 1.84 ms without it), 1
+//    issues Q K^T, 2 issues P V.  Warps 3-10 each sit
 //    on the tensor-memory lane quarter warp % 4.  On the quarters of the own
 //    heads, two warps run the softmax of each row, one per 32-column half
 //    (the two half-row maxima meet in shared memory).  On the quarters of
@@ -109,7 +110,6 @@ constexpr int kFirstRowWarp = 3;
 constexpr int kMlaThreads = 32 * (kFirstRowWarp + 8);  // 352
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384;
-constexpr int kPrefetch = 3;                           // stages prefetched into L2 ahead of the ring
 constexpr float kRescaleThreshold = 8.f;
 constexpr int kStuckMla = 1 << 20;
 
@@ -230,10 +230,9 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
         const int4 d = plan.item[it];
         const int b = d.x, r = d.y & 255, p0 = d.z, p1 = d.w;
         const int nst = (p1 - p0 + kSt - 1) / kSt;
-        // raw[i] = block-table entry of stage j + i
-        int32_t raw[kPrefetch + 2];
-#pragma unroll
-        for (int i = 0; i < kPrefetch + 2; ++i) raw[i] = i < nst ? bt_raw(b, r, p0, i) : -1;
+        // block-table entries of stages j and j + 1 (the next one is loaded a
+        // stage ahead of its use)
+        int32_t raw0 = nst > 0 ? bt_raw(b, r, p0, 0) : -1, raw1 = nst > 1 ? bt_raw(b, r, p0, 1) : -1;
         for (int j = 0; j < nst; ++j, ++g) {
           const uint32_t st = g % kNs, u = g / kNs;
           if (!mbar_wait(bars + 8 * (B_KV_EMPTY + st), (u & 1) ^ 1)) {
@@ -241,8 +240,8 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
             break;
           }
           const uint32_t full = bars + 8 * (B_KV_FULL + st);
-          if (usable(raw[0])) {
-            const int row = stage_row(raw[0], p0, j);
+          if (usable(raw0)) {
+            const int row = stage_row(raw0, p0, j);
             mbar_arrive_expect_tx(full, kStageBytes);
             const uint32_t dst = sbase + kKvOff + st * kStageBytes;
             for (int c = 0; c < 4; ++c)
@@ -252,18 +251,8 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
             if (crank == 0) count_error(A.err);
             mbar_arrive(full);
           }
-          // pull a later stage of this item into L2 so its load above finds it there
-#pragma unroll
-          for (int i = 1; i <= kPrefetch; ++i) {
-            if ((j == 0 || i == kPrefetch) && j + i < nst && usable(raw[i])) {
-              const int prow = stage_row(raw[i], p0, j + i);
-              for (int c = 0; c < 4; ++c) tma_prefetch_2d(&A.kvmap[r], xlat + 64 * c, prow);
-              tma_prefetch_2d(&A.ropemap[r], xrope, prow);
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < kPrefetch + 1; ++i) raw[i] = raw[i + 1];
-          raw[kPrefetch + 1] = j + kPrefetch + 2 < nst ? bt_raw(b, r, p0, j + kPrefetch + 2) : -1;
+          raw0 = raw1;
+          raw1 = j + 2 < nst ? bt_raw(b, r, p0, j + 2) : -1;
         }
       }
       if (dead) atomicAdd(errp, kStuckMla);

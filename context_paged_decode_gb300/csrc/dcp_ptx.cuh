@@ -311,14 +311,6 @@ __device__ __forceinline__ bool mbar_wait_relaxed_cluster(uint32_t bar, uint32_t
 
 
 
-// Prefetch one tile of a tensor map into L2 (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
-
 
 // Shared-memory matrix descriptor, 64-byte swizzle (rows of 64 bytes, 8-row
 // groups `sbo` apart): layout type 4 at [61,64).
