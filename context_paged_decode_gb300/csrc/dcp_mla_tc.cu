@@ -582,6 +582,19 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
       int prev_b = -1;
       bool dead = false;
       // bf16 P of my half-row relative to the maximum mb, and its sum
+      // (the first form for a half-row whose 32 tokens are all valid, the
+      // usual case; nv is the same across the warp)
+      auto make_p_full = [&](const float (&sc)[32], float mb, uint32_t (&pk)[16]) -> float {
+        float ls = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float pa = ex2_ftz(fmaf(sc[2 * e], A.sl2, -mb));
+          const float pq = ex2_ftz(fmaf(sc[2 * e + 1], A.sl2, -mb));
+          ls += pa + pq;
+          pk[e] = pack_bf16(pa, pq);
+        }
+        return ls;
+      };
       auto make_p = [&](const float (&sc)[32], int nv, float mb, uint32_t (&pk)[16]) -> float {
         float ls = 0.f;
 #pragma unroll
@@ -651,11 +664,16 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           if (armer) mbar_arrive_expect_tx_relaxed(bars + 8 * B_X_FULL, kXsBytes);
           // half-row maximum (raw scores; the scale is positive)
           float t16[16];
+          if (nv >= 32) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a = 2 * i < nv ? sc[2 * i] : -INFINITY;
-            const float c = 2 * i + 1 < nv ? sc[2 * i + 1] : -INFINITY;
-            t16[i] = fmaxf(a, c);
+            for (int i = 0; i < 16; ++i) t16[i] = fmaxf(sc[2 * i], sc[2 * i + 1]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float a = 2 * i < nv ? sc[2 * i] : -INFINITY;
+              const float c = 2 * i + 1 < nv ? sc[2 * i + 1] : -INFINITY;
+              t16[i] = fmaxf(a, c);
+            }
           }
 #pragma unroll
           for (int w = 8; w > 0; w >>= 1)
@@ -697,7 +715,8 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           }
           if (grow) m = mx;
           uint32_t pk[16];
-          const float ls = make_p(sc, nv, (m == -INFINITY) ? 0.f : m, pk);
+          const float mb = (m == -INFINITY) ? 0.f : m;
+          const float ls = nv >= 32 ? make_p_full(sc, mb, pk) : make_p(sc, nv, mb, pk);
           lh = lh * f + ls;
           const uint32_t pr = prow + sb * kPtBytes;
 #pragma unroll
