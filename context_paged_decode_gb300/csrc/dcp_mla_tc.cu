@@ -280,8 +280,8 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
         for (int j = 0; j < nst; ++j) {
           const uint32_t gs = g + j;
           const uint32_t st = gs % kNs, u = gs / kNs, sb = gs & 1, us = gs >> 1;
-          if (!mbar_wait(bars + 8 * (B_KV_FULL + st), u & 1) ||
-              !mbar_wait(bars + 8 * (B_S_FREE + sb), (us & 1) ^ 1)) {
+          if (!mbar_wait2_cluster(bars + 8 * (B_KV_FULL + st), u & 1, bars + 8 * (B_S_FREE + sb),
+                                  (us & 1) ^ 1)) {
             dead = true;
             break;
           }
