@@ -44,7 +44,10 @@
 //    (the two half-row maxima meet in shared memory).  On the quarters of
 //    the peer's heads, warps 3-6 ship the partial scores and warps 7-10
 //    receive the peer's P: they apply the peer's rescale factors to those
-//    rows of O and write those rows' output.  Shipping stages the scores in
+//    rows of O and write those rows' output.  P V waits for them only in the
+//    rare stages with a rescale; it reads the 64 factors itself.  Each
+//    receiver releases the peer's P slot (a remote arrival) once it has read
+//    the side entries.  Shipping stages the scores in
 //    shared memory and sends them with bulk copies: 16-byte remote stores
 //    would fill the SM's memory-instruction path, which the softmax's
 //    shared-memory loads and exp2 instructions also use;
@@ -104,7 +107,7 @@ constexpr int kSideOwnOff = kQRopeOff + kQRopeBytes;   // 216 KB
 constexpr int kSideRecvOff = kSideOwnOff + 2 * kSideBytes;
 constexpr int kMxOff = kSideRecvOff + 2 * kSideBytes;  // half-row maxima, [sb][half][row]
 constexpr int kBarOff = kMxOff + 3 * 2 * kOwn * 4;      // 221.5 KB
-constexpr int kNumBars = 28;
+constexpr int kNumBars = 29;
 constexpr int kMlaSmem = 1024 + kBarOff + kNumBars * 8 + 16;
 constexpr int kFirstRowWarp = 3;
 constexpr int kMlaThreads = 32 * (kFirstRowWarp + 8);  // 352
@@ -140,6 +143,7 @@ enum : int {
   B_Q_EMPTY = 23,
   B_O_FULL = 24,
   B_O_FREE = 25,
+  B_RS_DONE = 28,   // the receivers applied the peer's rescale factors (rescale stages only)
   B_MX = 26         // +own quarter: both halves of its rows stored their maxima (per stage,
                     // plus one phase per item for the row sums)
 };
@@ -148,10 +152,11 @@ constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kSt, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kDvHalf, false, true);
 
 __device__ __forceinline__ int arrivals(int i) {
-  if (i == B_S_FREE || i == B_S_FREE + 1 || i == B_O_FREE || i == B_P_FULL || i == B_P_FULL + 1)
-    return 6;
-  if (i == B_Q_FULL || i == B_XS_FREE) return 4;
-  if (i == B_PT_FREE || i == B_PT_FREE + 1 || i == B_MX || i == B_MX + 1) return 2;
+  if (i == B_S_FREE || i == B_S_FREE + 1 || i == B_O_FREE) return 6;
+  if (i == B_P_FULL || i == B_P_FULL + 1 || i == B_Q_FULL || i == B_XS_FREE) return 4;
+  // the P V of both CTAs (commits) and the peer's two receiver warps (remote)
+  if (i == B_PT_FREE || i == B_PT_FREE + 1) return 4;
+  if (i == B_MX || i == B_MX + 1 || i == B_RS_DONE) return 2;
   return 1;
 }
 
@@ -312,20 +317,36 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
     }
   } else if (warp == 2) {
     // ---------------- P V issuer ----------------
-    if (lane == 0) {
-      uint32_t g = 0, k = 0;
-      bool dead = false;
-      for (int it = i0; it < i1 && !dead; ++it, ++k) {
-        const int4 d = plan.item[it];
-        const int nst = (d.w - d.z + kSt - 1) / kSt;
-        for (int j = 0; j < nst; ++j) {
-          const uint32_t gs = g + j, st = gs % kNs, sb = gs & 1;
-          if (!mbar_wait(bars + 8 * (B_P_FULL + sb), (gs >> 1) & 1) ||
-              (j == 0 && !mbar_wait(bars + 8 * B_O_FREE, (k & 1) ^ 1))) {
+    // The whole warp waits; lane 0 issues.  P V of a stage needs this CTA's
+    // P rows (P_FULL, the four softmax warps) and the peer's (P_RECV, its bulk
+    // copies).  Only when the peer rescaled one of its rows does it also wait
+    // for the receivers to apply the rescale here (B_RS_DONE); the receivers
+    // and this warp count those stages from the same factors.
+    const uint32_t fside = sbase + kSideRecvOff + lane * 8;   // rows lane, lane + 32 (half 0)
+    uint32_t g = 0, k = 0, rsc = 0;
+    bool dead = false;
+    for (int it = i0; it < i1 && !dead; ++it, ++k) {
+      const int4 d = plan.item[it];
+      const int nst = (d.w - d.z + kSt - 1) / kSt;
+      for (int j = 0; j < nst; ++j) {
+        const uint32_t gs = g + j, st = gs % kNs, sb = gs & 1, us = gs >> 1;
+        if (!cwait2(bars + 8 * (B_P_FULL + sb), us & 1, bars + 8 * (B_P_RECV + sb), us & 1) ||
+            (j == 0 && !wwait(bars + 8 * B_O_FREE, (k & 1) ^ 1))) {
+          dead = true;
+          break;
+        }
+        float f0, f1;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(f0) : "r"(fside + sb * kSideBytes));
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(f1) : "r"(fside + sb * kSideBytes + 256));
+        if (__any_sync(0xffffffffu, f0 != 1.f || f1 != 1.f)) {
+          if (!wwait(bars + 8 * B_RS_DONE, rsc & 1)) {
             dead = true;
             break;
           }
-          tc_fence_after();
+          ++rsc;
+        }
+        tc_fence_after();
+        if (lane == 0) {
           // V = this CTA's four value chunks, the MN-major B operand: 64-column
           // atoms kChunkBytes apart, 8-token groups 1024 B apart; k-step kk
           // starts 16 tokens further.  P (K-major A operand) is P tile sb: two
@@ -343,12 +364,14 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
           // P tile sb of both CTAs may be rewritten once both P V have read it
           tc_commit_multicast(bars + 8 * (B_PT_FREE + sb), (uint16_t)3u);
         }
-        if (dead) break;
-        g += nst;
-        tc_commit(bars + 8 * B_O_FULL);
+        __syncwarp();
       }
-      if (dead) atomicAdd(errp, kStuckMla);
+      if (dead) break;
+      g += nst;
+      if (lane == 0) tc_commit(bars + 8 * B_O_FULL);
+      __syncwarp();
     }
+    if (dead && lane == 0) atomicAdd(errp, kStuckMla);
   } else {
     // ---------------- row warps: one tensor-memory lane (head) per thread ----------------
     const int q4 = warp & 3;                         // lane quarter = SM sub-partition
@@ -508,6 +531,8 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
     } else if (role == 2) {
       // ---------- receiver: the peer's P rows for its heads ----------
       const uint32_t side = sbase + kSideRecvOff + hp * 8;
+      const uint32_t fother = sbase + kSideRecvOff + (hp ^ 32) * 8;  // the other receiver's rows
+      const uint32_t ptfree_peer = mapa_shared(bars + 8 * B_PT_FREE, peer);
       const bool armer = lane == 0 && (q4 & 1) == 0;
       uint32_t g = 0, k = 0;
       bool dead = false;
@@ -524,26 +549,35 @@ mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
             dead = true;
             break;
           }
-          // side entries: (f, half-row sum) of half 0 and of half 1
-          float f, l0, l1;
+          // side entries: (f, half-row sum) of half 0 and of half 1, and the
+          // other receiver's factors (the P V warp decides on all 64 rows)
+          float f, l0, l1, fo;
           asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];"
                        : "=f"(f), "=f"(l0)
                        : "r"(side + sb * kSideBytes));
           asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l1) : "r"(side + sb * kSideBytes + kOwn * 8 + 4));
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(fo) : "r"(fother + sb * kSideBytes));
           lr = l0 + l1;   // both halves carry the same factor
           // the tile's next phase (stage gj + 2) expects the peer's bytes again
           if (armer) mbar_arrive_expect_tx_relaxed(bars + 8 * (B_P_RECV + sb), kPMsgBytes);
-          if (__any_sync(0xffffffffu, f != 1.f)) {
-            // wait for the P V of stage gj - 1 (in both CTAs), then rescale
+          // the side entries are read: the peer may refill this slot (its P of
+          // stage gj + 2).  The vote orders the remote arrival after the loads.
+          {
+            const uint32_t vote = __ballot_sync(0xffffffffu, f + l0 + l1 + fo > 0.f);
+            if (lane == 0) mbar_arrive_remote_relaxed(ptfree_peer + 8 * sb, __uint_as_float(vote));
+          }
+          if (__any_sync(0xffffffffu, f != 1.f || fo != 1.f)) {
+            // wait for the P V of stage gj - 1 (in both CTAs), rescale, and let
+            // the P V of stage gj go
             if (!cwait(bars + 8 * (B_PT_FREE + ((gj - 1) & 1)), ((gj - 1) >> 1) & 1)) {
               dead = true;
               break;
             }
             tc_fence_after();
             rescale_o(f, 0, kDvHalf / 32);
+            tc_fence_before();
+            warp_arrive(bars + 8 * B_RS_DONE);
           }
-          tc_fence_before();
-          warp_arrive(bars + 8 * (B_P_FULL + sb));
         }
         if (dead) break;
         g += nst;
