@@ -56,7 +56,7 @@ NCU_TRAFFIC = {
                      "kv_bytes": 282732 * 4096,
                      "capture": "profiles/gqa_tma_kernel_gqa_bf16_b32.md"},
     "mla_bf16_b64": {"source": "context_paged_decode_gb300/csrc/dcp_mla_tc.cu",
-                     "sha256_16": "eca2ecce6bd3c362", "dram_bytes": 251357440 + 5520384,
+                     "sha256_16": "4bca62db4a1b2bdf", "dram_bytes": 251376128 + 5723904,
                      "kv_bytes": 216885 * 1152,
                      "capture": "profiles/mla_tc_kernel_mla_bf16_b64.md"},
     "sfa_bf16_b32": {"source": "context_paged_decode_gb300/csrc/dcp_sfa_mma.cu",
