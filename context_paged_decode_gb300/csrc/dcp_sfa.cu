@@ -11,6 +11,7 @@
 
 #include "dcp_generic.cuh"
 #include "dcp_sfa_mma.cuh"
+#include "dcp_sfa_tc.cuh"
 
 using namespace dcp;
 
@@ -85,6 +86,34 @@ SfaMmaArgs sfa_mma_args(const dcp_layout_t& layout, const void* q, int B, int Hq
   return A;
 }
 
+bool sfa_tc_ok(const dcp_layout_t& layout, const void* q, int Hq, int dk, int dv,
+               dcp_dtype_t dtype, const dcp_paged_kv_t& kv, int K) {
+  return sfa_tc_supported(Hq, dk, dv, dtype, K, (int64_t)kv.num_blocks * layout.block_size, q,
+                          kv.k, layout.dcp_size);
+}
+
+SfaTcArgs sfa_tc_args(const dcp_layout_t& layout, int B, int Hq, float scale,
+                      const dcp_paged_kv_t& kv, int K, float* part_o, float* part_lse,
+                      int32_t* err) {
+  SfaTcArgs A;
+  memset(&A, 0, sizeof(A));
+  for (int r = 0; r < layout.dcp_size; ++r) A.pool[r] = (const uint8_t*)kv.k.ptr[r];
+  A.B = B;
+  A.Hq = Hq;
+  A.bs = layout.block_size;
+  A.K = K;
+  A.sl2 = scale * kLog2e;
+  A.num_blocks = kv.num_blocks;
+  A.bt = kv.block_table;
+  A.max_vb = kv.max_vblocks;
+  A.bt_rank_stride = kv.bt_rank_stride;
+  A.L = Layout{layout.dcp_size, layout.block_size, layout.interleave};
+  A.part_o = part_o;
+  A.part_lse = part_lse;
+  A.err = err;
+  return A;
+}
+
 }  // namespace
 
 extern "C" {
@@ -98,6 +127,13 @@ int dcp_sfa_decode_partial(dcp_layout_t layout, const void* q, int32_t num_reqs,
     return DCP_EINVAL;
   if (num_reqs == 0) return DCP_OK;
   if (!part_o || !part_lse || (topk_len > 0 && (!sel_rank || !sel_slot))) return DCP_EINVAL;
+  if (sfa_tc_ok(layout, q, num_q_heads, kv_dim, v_dim, dtype, kv, topk_len)) {
+    SfaTcArgs T = sfa_tc_args(layout, num_reqs, num_q_heads, scale, kv, topk_len, part_o, part_lse,
+                              err_count);
+    T.sel_rank = sel_rank;
+    T.sel_slot = sel_slot;
+    return launch_sfa_tc(T, q, layout.dcp_size, (cudaStream_t)stream);
+  }
   if (sfa_fast_ok(layout, q, num_q_heads, kv_dim, v_dim, dtype, kv, topk_len)) {
     SfaMmaArgs M = sfa_mma_args(layout, q, num_reqs, num_q_heads, scale, kv, topk_len, part_o,
                                 part_lse, err_count);
@@ -134,7 +170,13 @@ int dcp_sfa_decode(dcp_layout_t layout, const void* q, int32_t num_reqs, int32_t
                align_up(sizeof(float) * (size_t)dcp * num_reqs * num_q_heads * v_dim, 256));
   cudaStream_t s = (cudaStream_t)stream;
   int rc;
-  if (sfa_fast_ok(layout, q, num_q_heads, kv_dim, v_dim, dtype, kv, topk_len)) {
+  if (sfa_tc_ok(layout, q, num_q_heads, kv_dim, v_dim, dtype, kv, topk_len)) {
+    SfaTcArgs T = sfa_tc_args(layout, num_reqs, num_q_heads, scale, kv, topk_len, part_o, part_lse,
+                              err_count);
+    T.topk = topk;
+    T.seq_lens = seq_lens;
+    rc = launch_sfa_tc(T, q, layout.dcp_size, s);
+  } else if (sfa_fast_ok(layout, q, num_q_heads, kv_dim, v_dim, dtype, kv, topk_len)) {
     SfaMmaArgs M = sfa_mma_args(layout, q, num_reqs, num_q_heads, scale, kv, topk_len, part_o,
                                 part_lse, err_count);
     M.topk = topk;

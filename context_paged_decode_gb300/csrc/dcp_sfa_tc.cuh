@@ -1,0 +1,35 @@
+// tcgen05 SFA decode kernel: interface.
+#pragma once
+
+#include "dcp_common.cuh"
+#include "dcp_ptx.cuh"
+
+namespace dcp {
+
+struct SfaTcArgs {
+  CUtensorMap qmap;                     // q [B*Hq rows][576] bf16, box 64 x 64, 128 B swizzle
+  const uint8_t* pool[DCP_MAX_RANKS];   // per-rank latent pools [num_blocks*bs rows][576] bf16
+  int B, Hq, hblocks, bs, K;
+  float sl2;                            // softmax scale * log2(e)
+  int64_t num_blocks;
+  // selected tokens: remapped pairs, or global top-k remapped in the kernel
+  const int32_t* sel_rank;
+  const int32_t* sel_slot;
+  const int32_t* topk;
+  const int32_t* seq_lens;
+  const int32_t* bt;
+  int max_vb;
+  int64_t bt_rank_stride;
+  Layout L;
+  float* part_o;                        // [dcp][B][Hq][512]
+  float* part_lse;                      // [dcp][B][Hq]
+  int32_t* err;
+};
+
+// bf16, 576-wide latent rows with a 512-wide value, Hq a multiple of 64,
+// at most 2048 selected tokens per request, 16-byte aligned q and pools.
+bool sfa_tc_supported(int Hq, int dk, int dv, dcp_dtype_t dtype, int K, int64_t pool_rows,
+                      const void* q, const dcp_rank_ptrs_t& pool, int dcp);
+int launch_sfa_tc(const SfaTcArgs& A, const void* q, int dcp, cudaStream_t s);
+
+}  // namespace dcp
