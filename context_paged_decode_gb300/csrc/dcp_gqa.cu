@@ -19,6 +19,7 @@
 
 #include "dcp_generic.cuh"
 #include "dcp_ptx.cuh"
+#include "dcp_sfa_tc.cuh"
 
 namespace dcp {
 
@@ -462,9 +463,11 @@ int dcp_decode_workspace_size(dcp_layout_t layout, dcp_kind_t kind, int32_t num_
     return DCP_OK;
   }
   if (kind == DCP_KIND_SFA) {
-    // per-rank partials (o and lse) plus the remapped (rank, slot) pairs
+    // per-rank partials (o and lse) plus the remapped (rank, slot) pairs of
+    // the tensor-core path (at most 2048 selected tokens per request)
     *bytes = align_up(sizeof(float) * (size_t)dcp * num_reqs * num_q_heads * head_dim_v, 256) +
-             align_up(sizeof(float) * (size_t)dcp * num_reqs * num_q_heads, 256);
+             align_up(sizeof(float) * (size_t)dcp * num_reqs * num_q_heads, 256) +
+             2 * align_up(sizeof(int32_t) * (size_t)num_reqs * kSfaTcMaxSel, 256);
     return DCP_OK;
   }
   return DCP_EINVAL;

@@ -171,10 +171,19 @@ int dcp_sfa_decode(dcp_layout_t layout, const void* q, int32_t num_reqs, int32_t
   cudaStream_t s = (cudaStream_t)stream;
   int rc;
   if (sfa_tc_ok(layout, q, num_q_heads, kv_dim, v_dim, dtype, kv, topk_len)) {
+    // remap once per selected token, then every CTA of a request reads the pairs
+    int32_t* sel_rank =
+        (int32_t*)((char*)part_lse +
+                   align_up(sizeof(float) * (size_t)dcp * num_reqs * num_q_heads, 256));
+    int32_t* sel_slot =
+        (int32_t*)((char*)sel_rank + align_up(sizeof(int32_t) * (size_t)num_reqs * kSfaTcMaxSel, 256));
+    rc = dcp_sfa_remap(layout, topk, num_reqs, topk_len, seq_lens, kv.block_table, kv.max_vblocks,
+                       kv.bt_rank_stride, kv.num_blocks, sel_rank, sel_slot, err_count, stream);
+    if (rc) return rc;
     SfaTcArgs T = sfa_tc_args(layout, num_reqs, num_q_heads, scale, kv, topk_len, part_o, part_lse,
                               err_count);
-    T.topk = topk;
-    T.seq_lens = seq_lens;
+    T.sel_rank = sel_rank;
+    T.sel_slot = sel_slot;
     rc = launch_sfa_tc(T, q, layout.dcp_size, s);
   } else if (sfa_fast_ok(layout, q, num_q_heads, kv_dim, v_dim, dtype, kv, topk_len)) {
     SfaMmaArgs M = sfa_mma_args(layout, q, num_reqs, num_q_heads, scale, kv, topk_len, part_o,

@@ -60,7 +60,7 @@ constexpr int kPieces = kSt * kRowB / 16;              // 16-byte pieces per sta
 constexpr int kQOff = 0;
 constexpr int kSlotOff = kChunks * kHB * 128;          // 72 KB
 constexpr int kSelOff = kSlotOff + 2 * kStageB;        // 216 KB
-constexpr int kMaxSelTc = 2048;
+constexpr int kMaxSelTc = kSfaTcMaxSel;
 constexpr int kWMaxOff = kSelOff + kMaxSelTc * 4;      // [parity][warp][head] floats
 constexpr int kFacOff = kWMaxOff + 2 * 2 * kHB * 4;    // [parity][head] rescale factors
 constexpr int kMiscOff = kFacOff + 2 * kHB * 4;        // count, flags[2], rescale stage

@@ -6,6 +6,8 @@
 
 namespace dcp {
 
+constexpr int kSfaTcMaxSel = 2048;     // selected tokens per request on this path
+
 struct SfaTcArgs {
   CUtensorMap qmap;                     // q [B*Hq rows][576] bf16, box 64 x 64, 128 B swizzle
   const uint8_t* pool[DCP_MAX_RANKS];   // per-rank latent pools [num_blocks*bs rows][576] bf16

@@ -201,6 +201,8 @@ int dcp_gather_context_mla(dcp_layout_t layout, dcp_paged_kv_t kv, int32_t num_r
  * context lengths).  The caller allocates it; its contents need not be
  * initialised and are garbage afterwards.
  *  head_dim_v  value width (GQA head_dim; 512 for MLA / SFA).
+ * For DCP_KIND_SFA this includes 16 KB per request for the remapped
+ * (rank, slot) pairs of up to 2048 selected tokens.
  */
 int dcp_decode_workspace_size(dcp_layout_t layout, dcp_kind_t kind, int32_t num_reqs,
                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim_v,
