@@ -59,10 +59,10 @@ NCU_TRAFFIC = {
                      "sha256_16": "4bca62db4a1b2bdf", "dram_bytes": 251376128 + 5723904,
                      "kv_bytes": 216885 * 1152,
                      "capture": "profiles/mla_tc_kernel_mla_bf16_b64.md"},
-    "sfa_bf16_b32": {"source": "context_paged_decode_gb300/csrc/dcp_sfa_mma.cu",
-                     "sha256_16": "5e39c310216b018e", "dram_bytes": 78662400 + 4478976,
+    "sfa_bf16_b32": {"source": "context_paged_decode_gb300/csrc/dcp_sfa_tc.cu",
+                     "sha256_16": "eb7f9582acb4ec52", "dram_bytes": 78784512 + 3572992,
                      "kv_bytes": 32 * 2048 * 1152,
-                     "capture": "profiles/sfa_mma_kernel_sfa_bf16_b32.md"},
+                     "capture": "profiles/sfa_tc_kernel_sfa_bf16_b32.md"},
 }
 # the long-tail workloads run the same kernels
 NCU_TRAFFIC["longtail_gqa"] = NCU_TRAFFIC["gqa_bf16_b32"]
@@ -297,7 +297,7 @@ def run_ours(args, rank, world, local_rank):
             dcp.cache_write_mla(lay, newk, o_slot, wl.k_pools, wl.num_blocks)
         decode()
 
-    launches_per_step = 3 + (3 if cfg.kind != "sfa" else 2)
+    launches_per_step = 3 + 3
     kv_bytes, alg_bytes = step_bytes(cfg, wl.seq_lens_host, B)
     if cfg.kind == "sfa":
         kv_bytes = B * cfg.topk * cfg.dk * 2
