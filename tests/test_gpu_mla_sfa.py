@@ -187,3 +187,39 @@ def test_mla_online_softmax_rescale(lib, dcp_size):
         qv = W.as_float64(qb[0, h], "bf16")
         o_ref, lse_ref = O.attention(qv, K, K[:, :512], cfg.scale)
         ref.check_bf16(out[0, h], lse[0, h], o_ref, lse_ref, f"h{h}")
+
+
+@pytest.mark.parametrize("dcp_size", [1, 2])
+def test_sfa_online_softmax_rescale(lib, dcp_size):
+    """Selected tokens whose scores grow along the top-k order (and one
+    dominant late token) force the sparse kernel to rescale its output."""
+    import context_paged_decode_gb300 as dcp
+    import oracle as O
+    L, K = 3000, 1024
+    cfg = dataclasses.replace(SFA, B=1, lengths=[L], topk=K, dcp=dcp_size, bs=64, I=1)
+    rng = np.random.default_rng(12)
+    q = rng.standard_normal((1, cfg.Hq, 576)).astype(np.float32)
+    kv = rng.standard_normal((L, 576)).astype(np.float32)
+    sel = np.sort(rng.choice(L, K, replace=False)).astype(np.int32)
+    kv[sel] *= (1.0 + 3.0 * np.arange(K) / K)[:, None]     # every head rescales at least once
+    kv[sel[900]] = q[0, 5] * 0.2                          # dominates head 5
+    qb = W.f32_to_bf16_bits(q)
+    kvb = W.f32_to_bf16_bits(kv)
+    wl = D.build(cfg, populate=False)
+    wl.q.view(torch.int16).copy_(torch.from_numpy(qb.view(np.int16)))
+    req = torch.zeros(L, dtype=torch.int32, device="cuda")
+    pos = torch.arange(L, dtype=torch.int64, device="cuda")
+    _, slot = dcp.slot_mapping(wl.layout, req, pos, wl.block_table, wl.num_blocks)
+    kvd = torch.from_numpy(kvb.view(np.int16)).cuda().view(torch.bfloat16)
+    dcp.cache_write_mla(wl.layout, kvd, slot, wl.k_pools, wl.num_blocks)
+    topk = torch.from_numpy(sel[None, :].copy()).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = lib.sfa_decode(wl.layout, wl.q, wl.kv, topk, wl.seq_lens, cfg.scale, 512,
+                              out_dtype=torch.float32, err=err)
+    assert err.item() == 0
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    Ksel = W.as_float64(kvb, "bf16")[sel]
+    for h in [0, 5, 33, cfg.Hq - 1]:
+        qv = W.as_float64(qb[0, h], "bf16")
+        o_ref, lse_ref = O.attention(qv, Ksel, Ksel[:, :512], cfg.scale)
+        ref.check_bf16(out[0, h], lse[0, h], o_ref, lse_ref, f"h{h}")
