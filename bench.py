@@ -52,7 +52,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernel source is the one captured (sha256 prefix); otherwise null.
 NCU_TRAFFIC = {
     "gqa_bf16_b32": {"source": "context_paged_decode_gb300/csrc/dcp_gqa.cu",
-                     "sha256_16": "d84b9510e12045c1", "dram_bytes": 1159449344 + 6443264,
+                     "sha256_16": "a123735c3fb9abc0", "dram_bytes": 1159452000 + 7022592,
                      "kv_bytes": 282732 * 4096,
                      "capture": "profiles/gqa_tma_kernel_gqa_bf16_b32.md"},
     "mla_bf16_b64": {"source": "context_paged_decode_gb300/csrc/dcp_mla_tc.cu",
