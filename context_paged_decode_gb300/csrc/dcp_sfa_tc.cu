@@ -328,16 +328,24 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
         break;
       }
       const uint32_t dst0 = sbase + kSlotOff + slot * kStageB;
-#pragma unroll 4
-      for (int p = gt; p < kPieces; p += gthreads) {
-        // piece p: 16-byte unit c of token row rr; chunk c / 8, swizzled by rr & 7
-        const int rr = p / (kRowB / 16), c = p - rr * (kRowB / 16);
+      // a warp takes whole token rows (one slot-list read per row); lane l
+      // copies 16-byte units l, l + 32 and l + 64 (< 72) of the row: unit c
+      // goes to chunk c / 8, swizzled by rr & 7
+      const int gw_in = gt >> 5, gwarps = gthreads >> 5;
+#pragma unroll 2
+      for (int rr = gw_in; rr < kSt; rr += gwarps) {
         const int t = n * kSt + rr;
         const int row = t < n_sel ? sel[t] : -1;
-        const uint32_t dst =
-            dst0 + (c >> 3) * kChunkB + rr * 128 + ((uint32_t)((c & 7) ^ (rr & 7)) << 4);
-        const uint8_t* src = row >= 0 ? pool + (int64_t)row * kRowB + c * 16 : pool;
-        cp_async16_fill(dst, src, row >= 0 ? 16u : 0u);
+        const uint8_t* rsrc = row >= 0 ? pool + (int64_t)row * kRowB : pool;
+        const uint32_t bytes = row >= 0 ? 16u : 0u;
+        const uint32_t rdst = dst0 + rr * 128;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const int c = lane + 32 * k;
+          if (c < kRowB / 16)
+            cp_async16_fill(rdst + (c >> 3) * kChunkB + ((uint32_t)((c & 7) ^ (rr & 7)) << 4),
+                            row >= 0 ? rsrc + c * 16 : pool, bytes);
+        }
       }
       cp_async_commit();
       // the stage landed: make it visible to the tensor core
