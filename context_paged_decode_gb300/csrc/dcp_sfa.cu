@@ -104,10 +104,6 @@ SfaTcArgs sfa_tc_args(const dcp_layout_t& layout, int B, int Hq, float scale,
   A.K = K;
   A.sl2 = scale * kLog2e;
   A.num_blocks = kv.num_blocks;
-  A.bt = kv.block_table;
-  A.max_vb = kv.max_vblocks;
-  A.bt_rank_stride = kv.bt_rank_stride;
-  A.L = Layout{layout.dcp_size, layout.block_size, layout.interleave};
   A.part_o = part_o;
   A.part_lse = part_lse;
   A.err = err;

@@ -16,8 +16,8 @@
 //   O^T [512 value rows x 64 heads] += V_stage^T . P^T    (4 row blocks x 4 MMAs)
 // Shape of the kernel:
 //  * one CTA per (rank, request, 64 heads).  The CTA first lists its selected
-//    slots in top-k order (remapping global indices itself in the fused
-//    call), then walks them in 64-token stages through a two-slot ring;
+//    slots in top-k order (from the remapped (rank, slot) pairs), then walks
+//    them in 64-token stages through a two-slot ring;
 //  * shared memory: Q (64 heads x 576 as nine 8 KB chunks, 128-byte swizzle,
 //    one TMA box each), two 72 KB stage slots (nine 8 KB chunks of 64 token
 //    rows x 64 columns in the same layout) and the selection list.  The
@@ -128,16 +128,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Owner rank and in-block offset of global token x (< 2^31).
-__device__ __forceinline__ void place32(int x, const Layout& L, int& rank, int& vb, int& loc) {
-  const int vbs = L.bs * L.dcp;
-  vb = x / vbs;
-  const int off = x - vb * vbs;
-  const int lbi = off / L.I;
-  rank = lbi % L.dcp;
-  loc = (lbi / L.dcp) * L.I + off % L.I;
-}
-
 }  // namespace
 
 // Twelve warps put three on every SM sub-partition (16K registers each), so a
@@ -188,7 +178,7 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
     const int k0 = min(A.K, tid * per), k1 = min(A.K, k0 + per);
     int64_t slot[kPer];
     uint32_t own = 0;
-    if (A.topk == nullptr) {
+    {
       int rk[kPer];
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
@@ -199,34 +189,6 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
 #pragma unroll
       for (int i = 0; i < kPer; ++i)
         if (rk[i] == r) own |= 1u << i;
-    } else {
-      const int len = __ldg(A.seq_lens + b);
-      int gi[kPer];
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int k = k0 + i;
-        gi[i] = k < k1 ? __ldg(A.topk + (int64_t)b * A.K + k) : -1;
-      }
-      int loc[kPer];
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        int rk, vb;
-        loc[i] = 0;
-        slot[i] = -1;
-        if (gi[i] >= 0 && gi[i] < len) {
-          place32(gi[i], A.L, rk, vb, loc[i]);
-          if (rk == r) {
-            own |= 1u << i;
-            slot[i] = vb < A.max_vb ? (int64_t)__ldg(A.bt + r * A.bt_rank_stride +
-                                                     (int64_t)b * A.max_vb + vb)
-                                    : (int64_t)-1;
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kPer; ++i)
-        if (own >> i & 1)
-          slot[i] = (slot[i] >= 0 && slot[i] < A.num_blocks) ? slot[i] * A.bs + loc[i] : -2;
     }
     const int mine = __popc(own);
     __shared__ int wsum[kSfaTcThreads / 32];

@@ -14,15 +14,8 @@ struct SfaTcArgs {
   int B, Hq, hblocks, bs, K;
   float sl2;                            // softmax scale * log2(e)
   int64_t num_blocks;
-  // selected tokens: remapped pairs, or global top-k remapped in the kernel
-  const int32_t* sel_rank;
-  const int32_t* sel_slot;
-  const int32_t* topk;
-  const int32_t* seq_lens;
-  const int32_t* bt;
-  int max_vb;
-  int64_t bt_rank_stride;
-  Layout L;
+  const int32_t* sel_rank;               // [B][K] remapped owner rank (-1: not selected)
+  const int32_t* sel_slot;               // [B][K] slot on that rank
   float* part_o;                        // [dcp][B][Hq][512]
   float* part_lse;                      // [dcp][B][Hq]
   int32_t* err;
