@@ -20,7 +20,7 @@ from the definitions on the pages it cites:
   and mask non-owners; section "Decode computation": the attention sink is
   applied once when the partials are merged by log-sum-exp.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 
 * local in-block offset of token x on its rank:
   ``loc = (local_block_index // dcp) * I + offset_in_virtual_block % I`` and
