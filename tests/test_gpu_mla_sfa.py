@@ -223,3 +223,35 @@ def test_sfa_online_softmax_rescale(lib, dcp_size):
         qv = W.as_float64(qb[0, h], "bf16")
         o_ref, lse_ref = O.attention(qv, Ksel, Ksel[:, :512], cfg.scale)
         ref.check_bf16(out[0, h], lse[0, h], o_ref, lse_ref, f"h{h}")
+
+
+@pytest.mark.parametrize("hq", [64, 128])
+def test_sfa_bad_slots_are_counted_and_masked(lib, hq):
+    """(rank, slot) pairs whose slot lies outside the rank's cache are counted
+    once each and attended as masked tokens: the partials equal the oracle's
+    with those top-k entries dropped."""
+    cfg = dataclasses.replace(SFA, B=2, Hq=hq, lengths=[5000, 900], topk=256, dcp=4, bs=64, I=1)
+    wl = D.build(cfg)
+    topk = wl.topk_host.copy()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rk, sl = lib.sfa_remap(wl.layout, torch.from_numpy(topk).cuda(), wl.seq_lens, wl.block_table,
+                           wl.num_blocks, err=err)
+    assert err.item() == 0
+    rk_h, sl_h = rk.cpu().numpy(), sl.cpu().numpy()
+    bad = [(0, 3), (0, 100), (1, 7)]                      # (request, top-k index)
+    for b, k in bad:
+        assert rk_h[b, k] >= 0
+        sl_h[b, k] = wl.num_blocks * cfg.bs + 5           # beyond the rank's slots
+        topk[b, k] = -1                                   # the oracle drops it
+    po, pl = lib.sfa_decode_partial(wl.layout, wl.q, wl.kv, rk, torch.from_numpy(sl_h).cuda(),
+                                    cfg.scale, cfg.dv, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == len(bad)
+    po, pl = po.cpu().numpy(), pl.cpu().numpy()
+    for b in range(cfg.B):
+        heads = [0, 37, hq - 1]
+        exp = ref.sfa_expected(cfg, wl.seq_lens_host, topk, b, heads)
+        for h in heads:
+            _, _, po_ref, pl_ref = exp[h]
+            for r in range(cfg.dcp):
+                check(cfg, po[r, b, h], pl[r, b, h], po_ref[r], pl_ref[r], f"r{r} b{b} h{h}")
