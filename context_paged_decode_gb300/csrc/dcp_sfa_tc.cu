@@ -290,24 +290,24 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
         break;
       }
       const uint32_t dst0 = sbase + kSlotOff + slot * kStageB;
-      // a warp takes whole token rows (one slot-list read per row); lane l
-      // copies 16-byte units l, l + 32 and l + 64 (< 72) of the row: unit c
-      // goes to chunk c / 8, swizzled by rr & 7
+      // a warp takes groups of 4 token rows (one slot-list read per lane and
+      // group); each copy instruction moves chunk c of the 4 rows: lane l
+      // copies 16-byte unit l % 8 of row 4 g + l / 8, swizzled by the row & 7.
+      // All 32 lanes copy in every instruction: the load pipe's cost is per
+      // instruction, whatever its active lanes.
       const int gw_in = gt >> 5, gwarps = gthreads >> 5;
-#pragma unroll 2
-      for (int rr = gw_in; rr < kSt; rr += gwarps) {
+      const int rsub = lane >> 3, un = lane & 7;
+#pragma unroll 1
+      for (int rg = gw_in; rg < kSt / 4; rg += gwarps) {
+        const int rr = rg * 4 + rsub;
         const int t = n * kSt + rr;
         const int row = t < n_sel ? sel[t] : -1;
-        const uint8_t* rsrc = row >= 0 ? pool + (int64_t)row * kRowB : pool;
+        const uint8_t* rsrc = row >= 0 ? pool + (int64_t)row * kRowB + un * 16 : pool;
         const uint32_t bytes = row >= 0 ? 16u : 0u;
-        const uint32_t rdst = dst0 + rr * 128;
+        const uint32_t rdst = dst0 + rr * 128 + ((uint32_t)(un ^ (rr & 7)) << 4);
 #pragma unroll
-        for (int k = 0; k < 3; ++k) {
-          const int c = lane + 32 * k;
-          if (c < kRowB / 16)
-            cp_async16_fill(rdst + (c >> 3) * kChunkB + ((uint32_t)((c & 7) ^ (rr & 7)) << 4),
-                            row >= 0 ? rsrc + c * 16 : pool, bytes);
-        }
+        for (int c = 0; c < kChunks; ++c)
+          cp_async16_fill(rdst + c * kChunkB, row >= 0 ? rsrc + c * 128 : pool, bytes);
       }
       cp_async_commit();
       // the stage landed: make it visible to the tensor core
