@@ -102,6 +102,44 @@ def test_sfa_full_size_sampled(lib):
             ref.check_bf16(out[b, h], lse[b, h], exp[h][0], exp[h][1], f"b{b} h{h}")
 
 
+# The fused call on shapes the small cases miss: long per-rank selections
+# (16 stages of 64 tokens per rank), a whole context selected (exactly 8 stages
+# per rank) next to a request whose ranks 2 and 3 select nothing, 128 heads
+# (two CTAs per (rank, request)), and more (rank, request) problems than SMs.
+SFA_FUSED = [
+    dataclasses.replace(SFA, B=2, lengths=[60000, 9000], topk=2048, dcp=2),
+    dataclasses.replace(SFA, B=2, lengths=[2048, 100000], topk=2048, dcp=4),
+    dataclasses.replace(SFA, B=2, Hq=128, lengths=[20000, 4000], topk=1000, dcp=2),
+    dataclasses.replace(SFA, B=40, lengths=[600 + 97 * i for i in range(40)], topk=128, dcp=8),
+]
+
+
+@pytest.mark.parametrize("cfg", SFA_FUSED, ids=lambda c: f"B{c.B}-H{c.Hq}-dcp{c.dcp}-k{c.topk}")
+def test_sfa_fused_shapes(lib, cfg):
+    wl = D.build(cfg)
+    topk = wl.topk_host.copy()
+    if cfg.dcp == 4:
+        rank = (topk[1] % (cfg.bs * cfg.dcp)) // cfg.I % cfg.dcp
+        topk[1][rank >= 2] = -1
+    topk_d = torch.from_numpy(topk).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = lib.sfa_decode(wl.layout, wl.q, wl.kv, topk_d, wl.seq_lens, cfg.scale, cfg.dv,
+                              sink=wl.sink, out_dtype=torch.float32, err=err)
+    out2, lse2 = lib.sfa_decode(wl.layout, wl.q, wl.kv, topk_d, wl.seq_lens, cfg.scale, cfg.dv,
+                                sink=wl.sink, out_dtype=torch.float32, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(out, out2) and torch.equal(lse, lse2), "not bitwise repeatable"
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    sink = wl.sink.cpu().numpy()
+    reqs = range(cfg.B) if cfg.B <= 2 else [0, 17, cfg.B - 1]
+    for b in reqs:
+        heads = [0, 17, cfg.Hq - 1]
+        exp = ref.sfa_expected(cfg, wl.seq_lens_host, topk, b, heads, sink=sink)
+        for h in heads:
+            check(cfg, out[b, h], lse[b, h], exp[h][0], exp[h][1], f"b{b} h{h}")
+
+
 def mla_sampled(lib, cfg, reqs, heads_per_req, seed):
     wl = D.build(cfg)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -192,7 +230,11 @@ def test_mla_online_softmax_rescale(lib, dcp_size):
 @pytest.mark.parametrize("dcp_size", [1, 2])
 def test_sfa_online_softmax_rescale(lib, dcp_size):
     """Selected tokens whose scores grow along the top-k order (and one
-    dominant late token) force the sparse kernel to rescale its output."""
+    dominant late token) force the sparse kernel to rescale its output.
+    Only the 64 rope columns grow: the scores' spread rises more than
+    four-fold along the selection (every head's running maximum grows by more
+    than 8 in log2 one to three times), while the value columns stay N(0, 1),
+    so the output keeps the O(1) scale the bf16 tolerance is stated for."""
     import context_paged_decode_gb300 as dcp
     import oracle as O
     L, K = 3000, 1024
@@ -201,8 +243,8 @@ def test_sfa_online_softmax_rescale(lib, dcp_size):
     q = rng.standard_normal((1, cfg.Hq, 576)).astype(np.float32)
     kv = rng.standard_normal((L, 576)).astype(np.float32)
     sel = np.sort(rng.choice(L, K, replace=False)).astype(np.int32)
-    kv[sel] *= (1.0 + 3.0 * np.arange(K) / K)[:, None]     # every head rescales at least once
-    kv[sel[900]] = q[0, 5] * 0.2                          # dominates head 5
+    kv[sel, 512:] *= (1.0 + 12.0 * np.arange(K) / K)[:, None]
+    kv[sel[900]] = q[0, 5] * 0.8                          # dominates head 5
     qb = W.f32_to_bf16_bits(q)
     kvb = W.f32_to_bf16_bits(kv)
     wl = D.build(cfg, populate=False)
