@@ -5,7 +5,8 @@
 // parallelism", section "Decode computation" (the sink is applied once when
 // the partial outputs are merged by log-sum-exp):
 //     lse = ln(sum_i exp(lse_i) + exp(sink)),  o = sum_i exp(lse_i - lse) o_i.
-// HBM-bound: one warp per output row, 16-byte loads of the partials.
+// HBM-bound: one warp per output row (or per 128-value chunk of a row when
+// there are at most 16 parts), 16-byte loads of the partials.
 #include "dcp_common.cuh"
 
 namespace dcp {
@@ -267,6 +268,97 @@ __global__ void dense_plus_one_merge_kernel(int n, const float* __restrict__ po,
                 out_lse);
 }
 
+// The same merge with one warp per (output row, 128-value chunk), for calls
+// with at most NP parts: every part's LSE and its 128 values are loaded
+// before any is used, so a warp waits for memory once, and there are four
+// warps per 512-wide row to hide that wait.  The arithmetic and its order are
+// those of merge_row, so the output is bitwise the same.
+template <int NP, class Parts>
+__device__ __forceinline__ void merge_chunk(const Parts& P, int n, int64_t row, int dv, int chunk,
+                                            bool has_sink, float sink, void* out, int out_dtype,
+                                            int64_t out_row, float* out_lse) {
+  const int lane = threadIdx.x & 31;
+  const int nv = dv >> 2;
+  const int idx = chunk * 32 + lane;                 // float4 of the row
+  const bool act = idx < nv;
+  const float l_mine = lane < n ? P.lse_at(lane, row) : -INFINITY;
+  float4 v[NP];
+#pragma unroll
+  for (int i = 0; i < NP; ++i)
+    v[i] = (i < n && act) ? __ldg(reinterpret_cast<const float4*>(P.o_at(i, row, dv)) + idx)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+  float m = has_sink ? sink : -INFINITY;
+  m = fmaxf(m, l_mine);
+  m = warp_max(m);
+  if (m == -INFINITY) {  // nothing attended and no sink
+    if (act) {
+      if (out_dtype == DCP_F32)
+        reinterpret_cast<float4*>(out)[out_row * nv + idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+      else
+        reinterpret_cast<uint2*>(out)[out_row * nv + idx] = make_uint2(0u, 0u);
+    }
+    if (out_lse && chunk == 0 && lane == 0) out_lse[out_row] = -INFINITY;
+    return;
+  }
+  float s = l_mine != -INFINITY ? expf(l_mine - m) : 0.f;
+  s = warp_sum(s);
+  if (has_sink) s += expf(sink - m);
+  const float lse = m + logf(s);
+  const float wl = l_mine == -INFINITY ? 0.f : expf(l_mine - lse);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    const float w = __shfl_sync(0xffffffffu, wl, i);
+    if (i < n && w != 0.f) {  // an empty part adds nothing, whatever its o holds
+      acc.x = fmaf(w, v[i].x, acc.x);
+      acc.y = fmaf(w, v[i].y, acc.y);
+      acc.z = fmaf(w, v[i].z, acc.z);
+      acc.w = fmaf(w, v[i].w, acc.w);
+    }
+  }
+  if (act) {
+    if (out_dtype == DCP_F32)
+      reinterpret_cast<float4*>(out)[out_row * nv + idx] = acc;
+    else
+      reinterpret_cast<uint2*>(out)[out_row * nv + idx] =
+          make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
+  }
+  if (out_lse && chunk == 0 && lane == 0) out_lse[out_row] = lse;
+}
+
+template <int NP>
+__global__ void dense_merge_chunk_kernel(int n, const float* __restrict__ po,
+                                         const float* __restrict__ pl, int B, int H, int dv,
+                                         int chunks, const float* __restrict__ sink, void* out,
+                                         int out_dtype, float* out_lse) {
+  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t row = wid / chunks;
+  if (row >= (int64_t)B * H) return;
+  const int chunk = (int)(wid - row * chunks);
+  const int h = (int)(row % H);
+  DenseParts P{po, pl, (int64_t)B * H};
+  merge_chunk<NP>(P, n, row, dv, chunk, sink != nullptr, sink ? sink[h] : 0.f, out, out_dtype,
+                  row, out_lse);
+}
+
+template <int NP>
+__global__ void dense_plus_one_merge_chunk_kernel(int n, const float* __restrict__ po,
+                                                  const float* __restrict__ pl,
+                                                  const float* __restrict__ xo,
+                                                  const float* __restrict__ xl, int B, int H,
+                                                  int dv, int chunks,
+                                                  const float* __restrict__ sink, void* out,
+                                                  int out_dtype, float* out_lse) {
+  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t row = wid / chunks;
+  if (row >= (int64_t)B * H) return;
+  const int chunk = (int)(wid - row * chunks);
+  const int h = (int)(row % H);
+  DensePlusOne P{po, pl, (int64_t)B * H, n, xo, xl};
+  merge_chunk<NP>(P, n + 1, row, dv, chunk, sink != nullptr, sink ? sink[h] : 0.f, out,
+                  out_dtype, row, out_lse);
+}
+
 // mode 0: row = (b, h), parts = all items of (b, g) over every rank; sink applies.
 // mode 1: row = (r, b, h), parts = items of (b, g, r); output is float32 per rank.
 template <int CH>
@@ -363,9 +455,26 @@ extern "C" int dcp_lse_merge(int32_t num_parts, const float* part_o, const float
   if (rows == 0) return DCP_OK;
   if (!out || (num_parts > 0 && (!part_o || !part_lse))) return DCP_EINVAL;
   const int wpb = 8;
-  const unsigned grid = (unsigned)((rows + wpb - 1) / wpb);
   cudaStream_t st = (cudaStream_t)stream;
   const int nv = head_dim_v / 4;
+  if (num_parts <= 16) {
+    const int chunks = (nv + 31) / 32;
+    const unsigned cgrid = (unsigned)((rows * chunks + wpb - 1) / wpb);
+#define DCP_MERGE_CHUNK(NP)                                                               \
+  dense_merge_chunk_kernel<NP><<<cgrid, wpb * 32, 0, st>>>(num_parts, part_o, part_lse,   \
+                                                           num_reqs, num_heads, head_dim_v, \
+                                                           chunks, sink, out, (int)out_dtype, \
+                                                           out_lse)
+    if (num_parts <= 4)
+      DCP_MERGE_CHUNK(4);
+    else if (num_parts <= 8)
+      DCP_MERGE_CHUNK(8);
+    else
+      DCP_MERGE_CHUNK(16);
+#undef DCP_MERGE_CHUNK
+    return launch_status();
+  }
+  const unsigned grid = (unsigned)((rows + wpb - 1) / wpb);
   if (nv <= 32)
     dense_merge_kernel<1><<<grid, wpb * 32, 0, st>>>(num_parts, part_o, part_lse, num_reqs,
                                                      num_heads, head_dim_v, sink, out,
@@ -397,9 +506,25 @@ extern "C" int dcp_lse_merge_swa(int32_t num_parts, const float* part_o, const f
   if (rows == 0) return DCP_OK;
   if (!out || !swa_o || !swa_lse || (num_parts > 0 && (!part_o || !part_lse))) return DCP_EINVAL;
   const int wpb = 8;
-  const unsigned grid = (unsigned)((rows + wpb - 1) / wpb);
   cudaStream_t st = (cudaStream_t)stream;
   const int nv = head_dim_v / 4;
+  if (num_parts + 1 <= 16) {
+    const int chunks = (nv + 31) / 32;
+    const unsigned cgrid = (unsigned)((rows * chunks + wpb - 1) / wpb);
+#define DCP_MERGE_SWA_CHUNK(NP)                                                                  \
+  dense_plus_one_merge_chunk_kernel<NP><<<cgrid, wpb * 32, 0, st>>>(                             \
+      num_parts, part_o, part_lse, swa_o, swa_lse, num_reqs, num_heads, head_dim_v, chunks, sink, \
+      out, (int)out_dtype, out_lse)
+    if (num_parts + 1 <= 4)
+      DCP_MERGE_SWA_CHUNK(4);
+    else if (num_parts + 1 <= 8)
+      DCP_MERGE_SWA_CHUNK(8);
+    else
+      DCP_MERGE_SWA_CHUNK(16);
+#undef DCP_MERGE_SWA_CHUNK
+    return launch_status();
+  }
+  const unsigned grid = (unsigned)((rows + wpb - 1) / wpb);
 #define DCP_MERGE_SWA(CH)                                                                  \
   dense_plus_one_merge_kernel<CH><<<grid, wpb * 32, 0, st>>>(                              \
       num_parts, part_o, part_lse, swa_o, swa_lse, num_reqs, num_heads, head_dim_v, sink, \
