@@ -48,15 +48,23 @@ struct ItemParts {  // plan items: lse [item][G], o [item][G][dv]
   }
 };
 
+// Parts read per round of loads: 16 for rows of up to 128 values (one float4
+// per lane and part), fewer for wider rows, so a round holds 16 float4 per lane.
+template <int CH>
+constexpr int parts_per_round() {
+  return CH == 1 ? 16 : (CH == 2 ? 8 : 4);
+}
+
 // One warp per output row.  With at most 32 parts, lane i holds part i's
 // LSE, so the maximum, the sum and every part's weight come from one round
-// of loads and warp shuffles; the partial rows are then read four parts at
-// a time, all loads of a group issued before any is used.  More parts take
-// the same steps in blocks of 32.
+// of loads and warp shuffles; the partial rows are then read PG parts at a
+// time, all loads of a group issued before any is used.  More parts take the
+// same steps in blocks of 32.
 template <int CH, class Parts>
 __device__ __forceinline__ void merge_row(const Parts& P, int n, int64_t row, int dv,
                                           bool has_sink, float sink, void* out, int out_dtype,
                                           int64_t out_row, float* out_lse) {
+  constexpr int PG = parts_per_round<CH>();
   const int lane = threadIdx.x & 31;
   const int nv = dv >> 2;
   const float l_mine = lane < n ? P.lse_at(lane, row) : -INFINITY;
@@ -92,11 +100,11 @@ __device__ __forceinline__ void merge_row(const Parts& P, int n, int64_t row, in
       wl = l == -INFINITY ? 0.f : expf(l - lse);
     }
     const int cnt = min(32, n - blk);
-    for (int i0 = 0; i0 < cnt; i0 += 4) {
-      // up to four parts: every load first, then the weighted sums in part order
-      float4 v[4][CH];
+    for (int i0 = 0; i0 < cnt; i0 += PG) {
+      // up to PG parts: every load first, then the weighted sums in part order
+      float4 v[PG][CH];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < PG; ++q) {
         const float4* src =
             reinterpret_cast<const float4*>(P.o_at(blk + min(i0 + q, cnt - 1), row, dv));
 #pragma unroll
@@ -106,7 +114,7 @@ __device__ __forceinline__ void merge_row(const Parts& P, int n, int64_t row, in
         }
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < PG; ++q) {
         const float w = __shfl_sync(0xffffffffu, wl, min(i0 + q, 31));
         if (i0 + q < cnt && w != 0.f) {  // an empty part adds nothing, whatever its o holds
 #pragma unroll
@@ -147,6 +155,7 @@ __device__ __forceinline__ void merge_row_wide(const Parts& P, int n, int64_t ro
                                                int out_dtype, int64_t out_row, float* out_lse) {
   extern __shared__ float4 wide_acc[];               // [kWideWarps][nv]
   __shared__ float wm[kWideWarps], ws[kWideWarps];
+  constexpr int PG = parts_per_round<CH>();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int nv = dv >> 2;
   const int p0 = (int)((int64_t)n * w / kWideWarps), p1 = (int)((int64_t)n * (w + 1) / kWideWarps);
@@ -189,10 +198,10 @@ __device__ __forceinline__ void merge_row_wide(const Parts& P, int n, int64_t ro
       wl = l == -INFINITY ? 0.f : expf(l - lse);
     }
     const int cnt = min(32, p1 - blk);
-    for (int i0 = 0; i0 < cnt; i0 += 4) {
-      float4 v[4][CH];
+    for (int i0 = 0; i0 < cnt; i0 += PG) {
+      float4 v[PG][CH];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < PG; ++q) {
         const float4* src =
             reinterpret_cast<const float4*>(P.o_at(blk + min(i0 + q, cnt - 1), row, dv));
 #pragma unroll
@@ -202,7 +211,7 @@ __device__ __forceinline__ void merge_row_wide(const Parts& P, int n, int64_t ro
         }
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < PG; ++q) {
         const float wt = __shfl_sync(0xffffffffu, wl, min(i0 + q, 31));
         if (i0 + q < cnt && wt != 0.f) {
 #pragma unroll
