@@ -487,6 +487,38 @@ def run_ours(args, rank, world, local_rank):
 # CPU oracle timing (the reference arm, and the cpu_baseline of our arm)
 # ---------------------------------------------------------------------------
 
+def blas_threads():
+    """Threads numpy's BLAS runs with (the oracle's matmuls), else the host's
+    CPU count: threadpoolctl when installed, else the OpenBLAS that numpy
+    loaded, found in this process's memory map."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = sum(i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas")
+        if n > 0:
+            return n
+    except Exception:
+        pass
+    try:
+        import ctypes
+        import re
+        import numpy as np
+        np.dot(np.ones((64, 64)), np.ones((64, 64)))        # make sure the BLAS is loaded
+        with open("/proc/self/maps") as f:
+            paths = {m.group(1) for m in (re.search(r"(/\S*openblas\S*\.so\S*)", ln) for ln in f) if m}
+        for path in sorted(paths):
+            lib = ctypes.CDLL(path)
+            for name in ("openblas_get_num_threads", "openblas_get_num_threads64_",
+                         "scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads"):
+                fn = getattr(lib, name, None)
+                if fn is not None:
+                    n = int(fn())
+                    if n > 0:
+                        return n
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
 def oracle_sample(cfg, lens, budget_s, seed=0):
     """Time the fp64 oracle on whole (request, head) problems until budget_s of
     oracle compute; returns (KV bytes covered, seconds, description)."""
@@ -549,7 +581,7 @@ def run_reference(args, rank, world):
         "ms_per_step": round(1e3 * tot_s / max(1, args.steps), 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg.description, "name": cfg.name},
-        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": os.cpu_count(),
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": blas_threads(),
                          "kind": "oracle", "sample": f"per step: {what}"},
         "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -585,7 +617,7 @@ def main():
         if not args.no_cpu_baseline:
             b, s, what = oracle_sample(cfg, wl.seq_lens_host, args.cpu_budget)
             res["cpu_baseline"] = {"value": round(b / s / 1e9, 4), "unit": "GB/s",
-                                   "cores": os.cpu_count(), "kind": "oracle",
+                                   "cores": blas_threads(), "kind": "oracle",
                                    "sample": what + f", {s:.1f} s"}
         print(json.dumps(res), flush=True)
     if world > 1:
