@@ -164,6 +164,12 @@ int mla_max_items(int B, int dcp);
 
 // Merge item partials: mode 0 -> one output per (b, h) over all ranks (with
 // sink), mode 1 -> one output per (r, b, h) (no sink).
+// dcp_lse_merge for callers inside the library: with pdl, the launch is a
+// programmatic dependent of the previous kernel in the stream (the merge
+// waits for it before reading the partials).
+int launch_dense_merge(int num_parts, const float* part_o, const float* part_lse, int B, int H,
+                       int dv, const float* sink, void* out, int out_dtype, float* out_lse,
+                       cudaStream_t s, bool pdl);
 int launch_item_merge(const Plan& plan, int mode, int B, int dcp, int Hq, int G_per_item,
                       int groups, int dv, const float* sink, void* out, int out_dtype,
                       float* out_lse, cudaStream_t s);

@@ -10,6 +10,7 @@
 #include <stdlib.h>
 
 #include "dcp_common.cuh"
+#include "dcp_ptx.cuh"
 
 namespace dcp {
 
@@ -89,6 +90,7 @@ __global__ void sfa_remap_kernel(Layout L, const int32_t* __restrict__ topk, int
                                  int64_t bt_rank_stride, int64_t num_blocks,
                                  int32_t* __restrict__ out_rank, int32_t* __restrict__ out_slot,
                                  int32_t* err) {
+  griddep_launch_dependents();   // a dependent sparse-attention launch may start its prologue
   const int64_t n = (int64_t)B * K;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {

@@ -7,7 +7,10 @@
 //     lse = ln(sum_i exp(lse_i) + exp(sink)),  o = sum_i exp(lse_i - lse) o_i.
 // HBM-bound: one warp per output row (or per 128-value chunk of a row when
 // there are at most 16 parts), 16-byte loads of the partials.
+#include <utility>
+
 #include "dcp_common.cuh"
+#include "dcp_ptx.cuh"
 
 namespace dcp {
 
@@ -254,6 +257,7 @@ __global__ void dense_merge_kernel(int n, const float* __restrict__ po,
                                    const float* __restrict__ pl, int B, int H, int dv,
                                    const float* __restrict__ sink, void* out, int out_dtype,
                                    float* out_lse) {
+  griddep_wait();   // launched as a dependent: the partials are complete past this point
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= (int64_t)B * H) return;
   const int h = (int)(row % H);
@@ -340,6 +344,7 @@ __global__ void dense_merge_chunk_kernel(int n, const float* __restrict__ po,
                                          const float* __restrict__ pl, int B, int H, int dv,
                                          int chunks, const float* __restrict__ sink, void* out,
                                          int out_dtype, float* out_lse) {
+  griddep_wait();   // launched as a dependent: the partials are complete past this point
   const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t row = wid / chunks;
   if (row >= (int64_t)B * H) return;
@@ -453,6 +458,57 @@ int launch_item_merge(const Plan& plan, int mode, int B, int dcp, int Hq, int G,
 
 using namespace dcp;
 
+namespace dcp {
+
+namespace {
+
+template <typename... Exp, typename... Act>
+cudaError_t launch_maybe_pdl(bool pdl, void (*kernel)(Exp...), unsigned grid, unsigned block,
+                             cudaStream_t st, Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
+}
+
+}  // namespace
+
+int launch_dense_merge(int num_parts, const float* part_o, const float* part_lse, int B, int H,
+                       int dv, const float* sink, void* out, int out_dtype, float* out_lse,
+                       cudaStream_t st, bool pdl) {
+  const int64_t rows = (int64_t)B * H;
+  if (rows == 0) return DCP_OK;
+  const int wpb = 8;
+  const int nv = dv / 4;
+  cudaError_t e;
+  if (num_parts <= 16) {
+    const int chunks = (nv + 31) / 32;
+    const unsigned cgrid = (unsigned)((rows * chunks + wpb - 1) / wpb);
+    auto k = num_parts <= 4 ? dense_merge_chunk_kernel<4>
+             : num_parts <= 8 ? dense_merge_chunk_kernel<8> : dense_merge_chunk_kernel<16>;
+    e = launch_maybe_pdl(pdl, k, cgrid, wpb * 32, st, num_parts, part_o, part_lse, B, H, dv,
+                         chunks, sink, out, out_dtype, out_lse);
+  } else {
+    const unsigned grid = (unsigned)((rows + wpb - 1) / wpb);
+    auto k = nv <= 32 ? dense_merge_kernel<1>
+             : nv <= 64 ? dense_merge_kernel<2> : nv <= 128 ? dense_merge_kernel<4>
+                                                            : dense_merge_kernel<8>;
+    e = launch_maybe_pdl(pdl, k, grid, wpb * 32, st, num_parts, part_o, part_lse, B, H, dv, sink,
+                         out, out_dtype, out_lse);
+  }
+  if (e != cudaSuccess) return launch_status_report(e);
+  return launch_status();
+}
+
+}  // namespace dcp
+
 extern "C" int dcp_lse_merge(int32_t num_parts, const float* part_o, const float* part_lse,
                              int32_t num_reqs, int32_t num_heads, int32_t head_dim_v,
                              const float* sink, void* out, dcp_dtype_t out_dtype, float* out_lse,
@@ -463,44 +519,8 @@ extern "C" int dcp_lse_merge(int32_t num_parts, const float* part_o, const float
   const int64_t rows = (int64_t)num_reqs * num_heads;
   if (rows == 0) return DCP_OK;
   if (!out || (num_parts > 0 && (!part_o || !part_lse))) return DCP_EINVAL;
-  const int wpb = 8;
-  cudaStream_t st = (cudaStream_t)stream;
-  const int nv = head_dim_v / 4;
-  if (num_parts <= 16) {
-    const int chunks = (nv + 31) / 32;
-    const unsigned cgrid = (unsigned)((rows * chunks + wpb - 1) / wpb);
-#define DCP_MERGE_CHUNK(NP)                                                               \
-  dense_merge_chunk_kernel<NP><<<cgrid, wpb * 32, 0, st>>>(num_parts, part_o, part_lse,   \
-                                                           num_reqs, num_heads, head_dim_v, \
-                                                           chunks, sink, out, (int)out_dtype, \
-                                                           out_lse)
-    if (num_parts <= 4)
-      DCP_MERGE_CHUNK(4);
-    else if (num_parts <= 8)
-      DCP_MERGE_CHUNK(8);
-    else
-      DCP_MERGE_CHUNK(16);
-#undef DCP_MERGE_CHUNK
-    return launch_status();
-  }
-  const unsigned grid = (unsigned)((rows + wpb - 1) / wpb);
-  if (nv <= 32)
-    dense_merge_kernel<1><<<grid, wpb * 32, 0, st>>>(num_parts, part_o, part_lse, num_reqs,
-                                                     num_heads, head_dim_v, sink, out,
-                                                     (int)out_dtype, out_lse);
-  else if (nv <= 64)
-    dense_merge_kernel<2><<<grid, wpb * 32, 0, st>>>(num_parts, part_o, part_lse, num_reqs,
-                                                     num_heads, head_dim_v, sink, out,
-                                                     (int)out_dtype, out_lse);
-  else if (nv <= 128)
-    dense_merge_kernel<4><<<grid, wpb * 32, 0, st>>>(num_parts, part_o, part_lse, num_reqs,
-                                                     num_heads, head_dim_v, sink, out,
-                                                     (int)out_dtype, out_lse);
-  else
-    dense_merge_kernel<8><<<grid, wpb * 32, 0, st>>>(num_parts, part_o, part_lse, num_reqs,
-                                                     num_heads, head_dim_v, sink, out,
-                                                     (int)out_dtype, out_lse);
-  return launch_status();
+  return launch_dense_merge(num_parts, part_o, part_lse, num_reqs, num_heads, head_dim_v, sink,
+                            out, (int)out_dtype, out_lse, (cudaStream_t)stream, false);
 }
 
 extern "C" int dcp_lse_merge_swa(int32_t num_parts, const float* part_o, const float* part_lse,

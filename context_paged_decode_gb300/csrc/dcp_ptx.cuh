@@ -58,6 +58,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return false;
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream, when it was launched as a programmatic dependent, start before
+// this grid ends; wait blocks until the grid this one depends on has
+// completed and its memory is visible (a no-op without such a dependency).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

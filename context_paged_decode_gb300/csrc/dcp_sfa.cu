@@ -180,7 +180,12 @@ int dcp_sfa_decode(dcp_layout_t layout, const void* q, int32_t num_reqs, int32_t
                               err_count);
     T.sel_rank = sel_rank;
     T.sel_slot = sel_slot;
-    rc = launch_sfa_tc(T, q, layout.dcp_size, s);
+    // the remap, the partials and the merge overlap their launch boundaries:
+    // each dependent waits for its predecessor before reading its output
+    rc = launch_sfa_tc(T, q, layout.dcp_size, s, true);
+    if (rc) return rc;
+    return launch_dense_merge(dcp, part_o, part_lse, num_reqs, num_q_heads, v_dim, sink, out,
+                              (int)out_dtype, out_lse, s, true);
   } else if (sfa_fast_ok(layout, q, num_q_heads, kv_dim, v_dim, dtype, kv, topk_len)) {
     SfaMmaArgs M = sfa_mma_args(layout, q, num_reqs, num_q_heads, scale, kv, topk_len, part_o,
                                 part_lse, err_count);

@@ -149,6 +149,7 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
   const int64_t num_slots = A.num_blocks * A.bs;
   int32_t* errp = A.err;
 
+  griddep_launch_dependents();   // a dependent merge launch may start waiting
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) mbar_init(bars + 8 * i, arrivals(i));
     fence_mbar_init();
@@ -169,6 +170,9 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched as a dependent of the remap: its pairs are complete past this
+  // point (Q, a caller input, was ready before the remap started)
+  griddep_wait();
 
   // ---- this rank's selected slots, in top-k order (-1: unusable, attended as masked) ----
   {
@@ -618,7 +622,7 @@ bool sfa_tc_supported(int Hq, int dk, int dv, dcp_dtype_t dtype, int K, int64_t 
   return tensor_map_encoder() != nullptr;
 }
 
-int launch_sfa_tc(const SfaTcArgs& A0, const void* q, int dcp, cudaStream_t s) {
+int launch_sfa_tc(const SfaTcArgs& A0, const void* q, int dcp, cudaStream_t s, bool pdl) {
   SfaTcArgs A = A0;
   A.hblocks = A.Hq / kHB;
   if (!encode_q(&A.qmap, q, (uint64_t)A.B * A.Hq)) return DCP_ECUDA;
@@ -636,7 +640,18 @@ int launch_sfa_tc(const SfaTcArgs& A0, const void* q, int dcp, cudaStream_t s) {
   }
   const int grid = dcp * A.B * A.hblocks;
   if (grid <= 0) return DCP_OK;
-  sfa_tc_kernel<<<grid, kSfaTcThreads, kSfaTcSmem, s>>>(A);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kSfaTcThreads);
+  cfg.dynamicSmemBytes = kSfaTcSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, sfa_tc_kernel, A);
+  if (e != cudaSuccess) return launch_status_report(e);
   return launch_status();
 }
 

@@ -25,6 +25,9 @@ struct SfaTcArgs {
 // at most 2048 selected tokens per request, 16-byte aligned q and pools.
 bool sfa_tc_supported(int Hq, int dk, int dv, dcp_dtype_t dtype, int K, int64_t pool_rows,
                       const void* q, const dcp_rank_ptrs_t& pool, int dcp);
-int launch_sfa_tc(const SfaTcArgs& A, const void* q, int dcp, cudaStream_t s);
+// pdl: launched as a programmatic dependent of the previous kernel in the
+// stream, which must be the dcp_sfa_remap that produced sel_rank / sel_slot
+// (the kernel reads q and sets up before waiting for it).
+int launch_sfa_tc(const SfaTcArgs& A, const void* q, int dcp, cudaStream_t s, bool pdl = false);
 
 }  // namespace dcp
