@@ -181,8 +181,11 @@ int dcp_sfa_decode(dcp_layout_t layout, const void* q, int32_t num_reqs, int32_t
     T.sel_rank = sel_rank;
     T.sel_slot = sel_slot;
     // the remap, the partials and the merge overlap their launch boundaries:
-    // each dependent waits for its predecessor before reading its output
-    rc = launch_sfa_tc(T, q, layout.dcp_size, s, true);
+    // each dependent waits for its predecessor before reading its output.
+    // With no top-k entries the remap launches nothing, and the partials
+    // kernel must not overlap whatever the caller ran last.
+    const bool after_remap = (int64_t)num_reqs * topk_len > 0;
+    rc = launch_sfa_tc(T, q, layout.dcp_size, s, after_remap);
     if (rc) return rc;
     return launch_dense_merge(dcp, part_o, part_lse, num_reqs, num_q_heads, v_dim, sink, out,
                               (int)out_dtype, out_lse, s, true);

@@ -140,6 +140,38 @@ def test_sfa_fused_shapes(lib, cfg):
             check(cfg, out[b, h], lse[b, h], exp[h][0], exp[h][1], f"b{b} h{h}")
 
 
+@pytest.mark.parametrize("k_kind", ["no_entries", "padding_only"])
+@pytest.mark.parametrize("with_sink", [False, True])
+def test_sfa_empty_selection(lib, k_kind, with_sink):
+    """No selected token on any rank: the fused call (tensor-core path) and the
+    partial path give o = 0 with lse = the sink (or -inf without one), as the
+    oracle does."""
+    cfg = dataclasses.replace(SFA, B=2, lengths=[3000, 700], topk=64, dcp=4)
+    wl = D.build(cfg)
+    K = 0 if k_kind == "no_entries" else 64
+    topk = torch.full((cfg.B, K), -1, dtype=torch.int32, device="cuda")
+    sink = wl.sink if with_sink else None
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = lib.sfa_decode(wl.layout, wl.q, wl.kv, topk, wl.seq_lens, cfg.scale, cfg.dv,
+                              sink=sink, out_dtype=torch.float32, err=err)
+    rk, sl = lib.sfa_remap(wl.layout, topk, wl.seq_lens, wl.block_table, wl.num_blocks, err=err)
+    po, pl = lib.sfa_decode_partial(wl.layout, wl.q, wl.kv, rk, sl, cfg.scale, cfg.dv, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    out, lse, po, pl = (t.cpu().numpy() for t in (out, lse, po, pl))
+    sink_h = wl.sink.cpu().numpy() if with_sink else None
+    exp = ref.sfa_expected(cfg, wl.seq_lens_host, np.full((cfg.B, K), -1, np.int32), 0, [0, 63],
+                           sink=sink_h)
+    for h in (0, 63):
+        ref.check_bf16(out[0, h], lse[0, h], exp[h][0], exp[h][1], f"h{h}")
+    assert not out.any()
+    assert not po.any() and np.isneginf(pl).all()
+    if with_sink:
+        np.testing.assert_allclose(lse, np.broadcast_to(sink_h, lse.shape), rtol=0, atol=1e-6)
+    else:
+        assert np.isneginf(lse).all()
+
+
 def mla_sampled(lib, cfg, reqs, heads_per_req, seed):
     wl = D.build(cfg)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
