@@ -25,8 +25,15 @@ __global__ void cache_write_kernel(const uint4* __restrict__ src0, const uint4* 
     const uint4 a = __ldg(src0 + i);
     uint4 b = make_uint4(0, 0, 0, 0);
     if (NSRC == 2) b = __ldg(src1 + i);
-    for (int r = 0; r < dcp; ++r) {
-      const int64_t s = __ldg(slot + (int64_t)r * T + t);
+    // every rank's slot is loaded before any store, so the thread waits for
+    // memory once rather than once per rank
+    int64_t sl[DCP_MAX_RANKS];
+#pragma unroll
+    for (int r = 0; r < DCP_MAX_RANKS; ++r) sl[r] = r < dcp ? __ldg(slot + (int64_t)r * T + t) : -1;
+#pragma unroll
+    for (int r = 0; r < DCP_MAX_RANKS; ++r) {
+      if (r >= dcp) break;
+      const int64_t s = sl[r];
       if (s < 0 || s >= num_slots) {
         if (s != -1 && rem == 0) count_error(err);
         continue;
