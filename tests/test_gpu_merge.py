@@ -22,6 +22,7 @@ def test_merge_matches_oracle(lib, n, B, H, dv, with_sink):
     pl[rng.random((n, B, H)) < 0.2] = -np.inf
     if n > 1:
         pl[:, 0, 0] = -np.inf           # a row with every part empty
+    po[np.isneginf(pl)] = np.nan        # an empty part adds nothing, whatever its o holds
     sink = rng.standard_normal(H).astype(np.float32) if with_sink else None
     out, lse = lib.lse_merge(torch.from_numpy(po).cuda(), torch.from_numpy(pl).cuda(),
                              None if sink is None else torch.from_numpy(sink).cuda())

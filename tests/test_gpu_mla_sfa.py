@@ -172,6 +172,33 @@ def test_sfa_empty_selection(lib, k_kind, with_sink):
         assert np.isneginf(lse).all()
 
 
+def test_sfa_duplicate_indices_are_attended_as_listed(lib):
+    """The top-k list is taken literally: an index listed twice is attended
+    twice, by the fused call and the partial path alike, as by the oracle."""
+    cfg = dataclasses.replace(SFA, B=2, lengths=[5000, 900], topk=128, dcp=4)
+    wl = D.build(cfg)
+    topk = wl.topk_host.copy()
+    topk[0, 64:96] = topk[0, 0:32]          # 32 duplicates in request 0
+    topk[1, 1] = topk[1, 0]
+    topk_d = torch.from_numpy(topk).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = lib.sfa_decode(wl.layout, wl.q, wl.kv, topk_d, wl.seq_lens, cfg.scale, cfg.dv,
+                              sink=wl.sink, out_dtype=torch.float32, err=err)
+    rk, sl = lib.sfa_remap(wl.layout, topk_d, wl.seq_lens, wl.block_table, wl.num_blocks, err=err)
+    po, pl = lib.sfa_decode_partial(wl.layout, wl.q, wl.kv, rk, sl, cfg.scale, cfg.dv, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    out, lse, po, pl = (t.cpu().numpy() for t in (out, lse, po, pl))
+    sink = wl.sink.cpu().numpy()
+    for b in range(cfg.B):
+        exp = ref.sfa_expected(cfg, wl.seq_lens_host, topk, b, [0, 31, 63], sink=sink)
+        for h in (0, 31, 63):
+            o_ref, lse_ref, po_ref, pl_ref = exp[h]
+            ref.check_bf16(out[b, h], lse[b, h], o_ref, lse_ref, f"fused b{b} h{h}")
+            for r in range(cfg.dcp):
+                ref.check_bf16(po[r, b, h], pl[r, b, h], po_ref[r], pl_ref[r], f"r{r} b{b} h{h}")
+
+
 def mla_sampled(lib, cfg, reqs, heads_per_req, seed):
     wl = D.build(cfg)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
