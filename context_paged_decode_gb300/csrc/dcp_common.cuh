@@ -152,12 +152,13 @@ int launch_plan(const int32_t* local_lens, int B, int dcp, int G, int tile, int 
                 int target_items, const Plan& plan, cudaStream_t s);
 
 // Balanced-parts plan (G = 1): the local ranges of all (b, r), concatenated in
-// (b, r) order, are cut into `parts` runs of about equal token count; a cut
-// inside a range falls on a multiple of `tile` positions.  Items are the
-// pieces between cuts, in (b, r) order; run k owns items
+// (b, r) order, are cut into `parts` runs of about equal cost, where a
+// non-empty range costs its tokens plus `overhead` (the fixed cost of an item,
+// in tokens); a cut inside a range falls on a multiple of `tile` positions.
+// Items are the pieces between cuts, in (b, r) order; run k owns items
 // [pfirst[k], pfirst[k+1]).  At most B*dcp + parts - 1 items; 1 <= parts <= kMaxParts.
 int launch_plan_parts(const int32_t* local_lens, int B, int dcp, int tile, int parts,
-                      const Plan& plan, cudaStream_t s);
+                      int overhead, const Plan& plan, cudaStream_t s);
 
 // Largest item count the MLA plan can produce (sizes its workspace).
 int mla_max_items(int B, int dcp);

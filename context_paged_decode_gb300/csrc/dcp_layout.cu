@@ -253,14 +253,17 @@ __device__ __forceinline__ int64_t block_scan_excl_i64(int64_t v, int64_t* sh, i
 // at most one run and no run boundary splits a tile).
 __global__ void __launch_bounds__(kPlanThreads)
 plan_parts_kernel(const int32_t* __restrict__ local_lens, int B, int dcp, int tile, int parts,
-                  Plan plan) {
+                  int overhead, Plan plan) {
   __shared__ int64_t sh64[33];
   __shared__ int sh[32];
   const int n = B * dcp;
   const int per_thr = (n + blockDim.x - 1) / blockDim.x;
   const int e0 = min(n, (int)threadIdx.x * per_thr), e1 = min(n, e0 + per_thr);
   int64_t mine = 0;
-  for (int e = e0; e < e1; ++e) mine += max(local_lens[e], 0);
+  for (int e = e0; e < e1; ++e) {
+    const int64_t len = max(local_lens[e], 0);
+    mine += len > 0 ? len + overhead : 0;
+  }
   int64_t tot;
   const int64_t start0 = block_scan_excl_i64(mine, sh64, &tot);
   int64_t per = (tot + parts - 1) / parts;
@@ -273,10 +276,11 @@ plan_parts_kernel(const int32_t* __restrict__ local_lens, int B, int dcp, int ti
     for (int e = e0; e < e1; ++e) {
       const int64_t len = max(local_lens[e], 0);
       if (len > 0) {
-        const int64_t last = S + (len - 1) / tile * tile;
-        cnt += (int)(last / per - S / per + 1);
+        const int64_t S0 = S + overhead;       // position of the entry's first token
+        const int64_t last = S0 + (len - 1) / tile * tile;
+        cnt += (int)(last / per - S0 / per + 1);
+        S += len + overhead;
       }
-      S += len;
     }
   }
   int total;
@@ -288,11 +292,12 @@ plan_parts_kernel(const int32_t* __restrict__ local_lens, int B, int dcp, int ti
       const int64_t len = max(local_lens[e], 0);
       plan.off[e] = min(base, plan.max_items);
       if (len > 0) {
+        const int64_t S0 = S + overhead;
         const int64_t ntiles = (len + tile - 1) / tile;
-        const int64_t kf = S / per, kl = (S + (ntiles - 1) * tile) / per;
+        const int64_t kf = S0 / per, kl = (S0 + (ntiles - 1) * tile) / per;
         for (int64_t k = kf; k <= kl; ++k) {
-          const int64_t t0 = k == kf ? 0 : (k * per - S + tile - 1) / tile;
-          const int64_t t1 = k == kl ? ntiles : ((k + 1) * per - S + tile - 1) / tile;
+          const int64_t t0 = k == kf ? 0 : (k * per - S0 + tile - 1) / tile;
+          const int64_t t1 = k == kl ? ntiles : ((k + 1) * per - S0 + tile - 1) / tile;
           if (base < plan.max_items) {
             plan.item[base] = make_int4(e / dcp, e % dcp, (int)(t0 * tile),
                                         (int)(t1 * tile < len ? t1 * tile : len));
@@ -300,8 +305,8 @@ plan_parts_kernel(const int32_t* __restrict__ local_lens, int B, int dcp, int ti
           }
           ++base;
         }
+        S += len + overhead;
       }
-      S += len;
     }
   }
   __syncthreads();
@@ -322,9 +327,9 @@ plan_parts_kernel(const int32_t* __restrict__ local_lens, int B, int dcp, int ti
 }
 
 int launch_plan_parts(const int32_t* local_lens, int B, int dcp, int tile, int parts,
-                      const Plan& plan, cudaStream_t s) {
-  if (parts < 1 || parts > kMaxParts || tile < 1) return DCP_EINVAL;
-  plan_parts_kernel<<<1, kPlanThreads, 0, s>>>(local_lens, B, dcp, tile, parts, plan);
+                      int overhead, const Plan& plan, cudaStream_t s) {
+  if (parts < 1 || parts > kMaxParts || tile < 1 || overhead < 0) return DCP_EINVAL;
+  plan_parts_kernel<<<1, kPlanThreads, 0, s>>>(local_lens, B, dcp, tile, parts, overhead, plan);
   return launch_status();
 }
 
