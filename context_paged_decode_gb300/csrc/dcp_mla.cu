@@ -19,8 +19,8 @@ int mla_target_items() { return 4 * num_sms(); }
 // What an item costs a cluster beyond its tokens (Q reload, epilogue and
 // ring refill), in tokens, for balancing the runs of the tensor-core kernel.
 // On GB300 (B=64, 128 heads, bimodal lengths, 3-22 items per run) a step took
-// 1.770 ms with runs of equal tokens, 1.707 ms at 256, 1.674 ms at 512 and
-// 1.707 ms at 1024.
+// 1.770 ms with runs of equal tokens; 1.707, 1.677, 1.670, 1.677, 1.687 and
+// 1.707 ms at 256, 384, 512, 640, 768 and 1024.
 constexpr int kMlaItemOverhead = 512;
 
 // The balanced-parts plan makes at most B*dcp + clusters - 1 items and the
