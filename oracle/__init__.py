@@ -209,6 +209,28 @@ def attention(q, K, V, scale):
     return o, lse
 
 
+def attention_heads(Q, K, V, scale):
+    """Softmax attention of several queries over one key set, fp64.
+
+    The definition of ``attention`` applied to every row of Q[h, dk] (the
+    query heads that share one KV head, or every head of an MLA latent):
+    S[j, h] = scale * q_h.k_j, lse_h = ln sum_j exp(S[j, h]),
+    o_h = sum_j exp(S[j, h] - lse_h) v_j.  Returns (O[h, dv], lse[h]); an
+    empty key set gives zeros and -inf for every head.
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    nh = Q.shape[0]
+    if K.shape[0] == 0:
+        return np.zeros((nh, V.shape[1]), dtype=np.float64), np.full(nh, NEG_INF)
+    S = scale * (K @ Q.T)
+    m = S.max(axis=0)
+    lse = m + np.log(np.exp(S - m).sum(axis=0))
+    O = np.exp(S - lse).T @ V
+    return O, lse
+
+
 def shard_tokens(L, r, dcp, bs, I):
     """Global token ids owned by rank r among [0, L), in local-position order."""
     n = local_seq_len_closed_form(L, r, dcp, bs, I)
@@ -257,6 +279,30 @@ def sharded_attention(q, K_all, V_all, scale, L, dcp, bs, I, sink=None):
     return o, lse, po, pl
 
 
+def sharded_attention_heads(Q, K_all, V_all, scale, L, dcp, bs, I, sinks=None):
+    """``sharded_attention`` for several query heads over the same keys.
+
+    Q[h, dk]; K_all/V_all hold the request's keys/values in global token
+    order; sinks: None or one logit per row of Q.  Each rank attends its own
+    shard ("Decode": attention over the local KV), then each head's partials
+    are merged by log-sum-exp with its sink applied once.  Returns
+    (o[h, dv], lse[h], per_rank_o[dcp, h, dv], per_rank_lse[dcp, h]).
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    nh, dv = Q.shape[0], V_all.shape[1]
+    po = np.zeros((dcp, nh, dv))
+    pl = np.full((dcp, nh), NEG_INF)
+    for r in range(dcp):
+        idx = shard_tokens(L, r, dcp, bs, I)
+        po[r], pl[r] = attention_heads(Q, K_all[idx], V_all[idx], scale)
+    o = np.zeros((nh, dv))
+    lse = np.full(nh, NEG_INF)
+    for h in range(nh):
+        s = None if sinks is None else float(sinks[h])
+        o[h], lse[h] = lse_merge(po[:, h], pl[:, h], s)
+    return o, lse, po, pl
+
+
 def sparse_attention(q, K_all, V_all, scale, sel):
     """Attention restricted to the selected global token ids (SFA, unsharded)."""
     sel = np.asarray([g for g in sel if g >= 0 and g < K_all.shape[0]], dtype=np.int64)
@@ -274,6 +320,38 @@ def sfa_sharded(q, K_all, V_all, scale, sel, L, dcp, bs, I, sink=None):
         mine = sel[owners == r]
         po[r], pl[r] = attention(q, K_all[mine], V_all[mine], scale)
     o, lse = lse_merge(po, pl, sink)
+    return o, lse, po, pl
+
+
+def sfa_sharded_heads(Q, sel, K_sel, V_sel, scale, L, dcp, bs, I, sinks=None):
+    """``sfa_sharded`` for several query heads, given only the selected rows.
+
+    sel[k] are the global top-k token ids of the request and K_sel[k] /
+    V_sel[k] the key / value rows of token sel[k] (so a long context need
+    not be materialised).  Entries outside [0, L) are dropped; every other
+    entry is attended as listed by the rank that owns it ("GLM-5.2 SFA DCP
+    replicated indexer": each rank attends the selected tokens it holds);
+    the partials are merged per head with its sink applied once.  Returns
+    (o[h, dv], lse[h], per_rank_o[dcp, h, dv], per_rank_lse[dcp, h]).
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    sel = np.asarray(sel, dtype=np.int64)
+    keep = (sel >= 0) & (sel < L)
+    sel = sel[keep]
+    K_sel = np.asarray(K_sel)[keep]
+    V_sel = np.asarray(V_sel)[keep]
+    owners = target_rank(sel, bs, dcp, I)
+    nh, dv = Q.shape[0], V_sel.shape[1]
+    po = np.zeros((dcp, nh, dv))
+    pl = np.full((dcp, nh), NEG_INF)
+    for r in range(dcp):
+        mine = owners == r
+        po[r], pl[r] = attention_heads(Q, K_sel[mine], V_sel[mine], scale)
+    o = np.zeros((nh, dv))
+    lse = np.full(nh, NEG_INF)
+    for h in range(nh):
+        s = None if sinks is None else float(sinks[h])
+        o[h], lse[h] = lse_merge(po[:, h], pl[:, h], s)
     return o, lse, po, pl
 
 

@@ -392,3 +392,96 @@ def test_gather_context_inverts_the_cache_write():
         # unresolvable tokens give zero rows
         out, bad = O.gather_context([0, 5], [10 ** 6, 0], caches, bt, dcp, bs, I, nb)
         assert bad == 2 and (out == 0).all()
+
+
+# ---------------------------------------------------------------------------
+# several query heads over one key set (the full-size parity checks use
+# these): pinned against scipy per head and the procedural dealing, not
+# against the single-head oracle functions
+# ---------------------------------------------------------------------------
+
+def scipy_attention(q, K, V, scale):
+    s = scale * np.einsum("d,nd->n", q, K)
+    return scipy.special.softmax(s) @ V, scipy.special.logsumexp(s)
+
+
+def test_attention_heads_against_library_routines():
+    rng = np.random.default_rng(21)
+    for nh, n, dk, dv in [(1, 1, 4, 4), (4, 300, 64, 64), (3, 33, 576, 512), (5, 2, 8, 3)]:
+        Q, K, V = rnd(rng, nh, dk), rnd(rng, n, dk), rnd(rng, n, dv)
+        o, lse = O.attention_heads(Q, K, V, 0.41)
+        assert o.shape == (nh, dv) and lse.shape == (nh,)
+        for h in range(nh):
+            o_ref, l_ref = scipy_attention(Q[h], K, V, 0.41)
+            np.testing.assert_allclose(o[h], o_ref, rtol=1e-12, atol=1e-13)
+            assert lse[h] == pytest.approx(l_ref, rel=1e-13, abs=1e-13)
+    # one key: every head gets v and its own score
+    Q, k, v = rnd(rng, 3, 8), rnd(rng, 8), rnd(rng, 5)
+    o, lse = O.attention_heads(Q, k[None], v[None], 0.5)
+    for h in range(3):
+        np.testing.assert_allclose(o[h], v, rtol=1e-14)
+        assert lse[h] == pytest.approx(0.5 * float(Q[h] @ k), rel=1e-14)
+    # no keys
+    o, lse = O.attention_heads(Q, np.zeros((0, 8)), np.zeros((0, 5)), 1.0)
+    assert (o == 0).all() and (lse == -math.inf).all()
+
+
+@pytest.mark.parametrize("dcp,bs,I", [(1, 16, 1), (8, 16, 1), (3, 8, 4), (8, 64, 64), (4, 4, 2)])
+def test_sharded_attention_heads_against_dealing_and_scipy(dcp, bs, I):
+    """Per-rank partials equal scipy attention over the tokens the procedural
+    dealing gives each rank; the merged result equals scipy attention over
+    all keys plus, with a sink, one extra key of logit sigma_h and zero value."""
+    rng = np.random.default_rng(dcp * 7 + bs + I)
+    nh, dk, dv, scale = 4, 16, 12, 0.3
+    for L in [1, dcp, bs * dcp + 1, 500]:
+        Q, K, V = rnd(rng, nh, dk), rnd(rng, L, dk), rnd(rng, L, dv)
+        sinks = rnd(rng, nh)
+        local = deal_tokens(L, dcp, bs, I)
+        for with_sink in (False, True):
+            o, lse, po, pl = O.sharded_attention_heads(Q, K, V, scale, L, dcp, bs, I,
+                                                       sinks=sinks if with_sink else None)
+            for h in range(nh):
+                for r in range(dcp):
+                    if not local[r]:
+                        assert pl[r, h] == -math.inf and (po[r, h] == 0).all()
+                        continue
+                    o_r, l_r = scipy_attention(Q[h], K[local[r]], V[local[r]], scale)
+                    np.testing.assert_allclose(po[r, h], o_r, rtol=1e-12, atol=1e-13)
+                    assert pl[r, h] == pytest.approx(l_r, rel=1e-13, abs=1e-13)
+                s = scale * (K @ Q[h])
+                if with_sink:
+                    s = np.r_[s, sinks[h]]
+                w = scipy.special.softmax(s)[:L]
+                np.testing.assert_allclose(o[h], w @ V, rtol=1e-11, atol=1e-13)
+                assert lse[h] == pytest.approx(scipy.special.logsumexp(s), rel=1e-13, abs=1e-13)
+
+
+def test_sfa_sharded_heads_against_dealing_and_scipy():
+    """Only the selected rows are given; entries outside [0, L) are dropped;
+    each valid entry (duplicates included) is attended once, by the rank the
+    procedural dealing gives its token; the merge applies each head's sink once."""
+    rng = np.random.default_rng(33)
+    dcp, bs, I, L = 4, 8, 8, 700
+    nh, dk, dv, scale = 3, 20, 16, 0.25
+    owner = np.empty(L, dtype=np.int64)
+    for r, toks in enumerate(deal_tokens(L, dcp, bs, I)):
+        owner[toks] = r
+    sel = np.r_[rng.choice(L, 60, replace=False), [-1, L, 5, 5]]
+    Ksel, Vsel = rnd(rng, len(sel), dk), rnd(rng, len(sel), dv)
+    Ksel[-1], Vsel[-1] = Ksel[-2], Vsel[-2]         # the duplicate carries the same row
+    Q, sinks = rnd(rng, nh, dk), rnd(rng, nh)
+    o, lse, po, pl = O.sfa_sharded_heads(Q, sel, Ksel, Vsel, scale, L, dcp, bs, I, sinks=sinks)
+    valid = (sel >= 0) & (sel < L)
+    for h in range(nh):
+        for r in range(dcp):
+            m = valid & (owner[np.clip(sel, 0, L - 1)] == r)
+            if not m.any():
+                assert pl[r, h] == -math.inf
+                continue
+            o_r, l_r = scipy_attention(Q[h], Ksel[m], Vsel[m], scale)
+            np.testing.assert_allclose(po[r, h], o_r, rtol=1e-12, atol=1e-13)
+            assert pl[r, h] == pytest.approx(l_r, rel=1e-13)
+        s = np.r_[scale * (Ksel[valid] @ Q[h]), sinks[h]]
+        w = scipy.special.softmax(s)[:-1]
+        np.testing.assert_allclose(o[h], w @ Vsel[valid], rtol=1e-11, atol=1e-13)
+        assert lse[h] == pytest.approx(scipy.special.logsumexp(s), rel=1e-13)
