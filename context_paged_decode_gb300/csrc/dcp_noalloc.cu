@@ -8,12 +8,20 @@
 // split-KV workspace taken from a fixed array in the library's own device
 // memory instead of a caller buffer.
 //
-// The array is a file-scope __device__ object of kNoallocScratchBytes; every
-// GPU that loads the library holds it until the process exits.  Host code
-// may not use its name as a device address, so its address is looked up with
-// cudaGetSymbolAddress once per device (on the first call made on that
-// device, with that device current) and passed to the kernels like any
-// workspace.  No call here allocates memory.
+// The array is a file-scope __device__ object of kNoallocScratchBytes.  The
+// library's device code is loaded lazily, so the array is reserved on a
+// device by the first call made there (the cudaGetSymbolAddress below loads
+// this file's module); from then on the device holds it until the process
+// exits.  That first call returns DCP_ECUDA when the 16 MiB cannot be
+// reserved, and it should come before any stream capture, as a warm-up.
+// Host code may not use the array's name as a device address, so the address
+// is looked up with cudaGetSymbolAddress, with the device current, and passed
+// to the kernels like any workspace.  It is cached per device together with
+// the unique id of the CUDA context it was looked up in; a call made in
+// another context (after cudaDeviceReset, or under a context the caller
+// created) looks it up again.  No call here allocates memory.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "dcp_common.cuh"
@@ -25,21 +33,55 @@ constexpr size_t kNoallocScratchBytes = size_t(16) << 20;  // 16 MiB
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
+struct ScratchSlot {
+  void* ptr = nullptr;
+  unsigned long long ctx_id = 0;
+  bool keyed = false;  // ctx_id is valid
+};
+ScratchSlot g_scratch[kMaxDevices];
 std::mutex g_scratch_mu;
 
-// Device address of the scratch array on the current device (looked up once).
+// cuCtxGetId through the runtime's driver entry point (no -lcuda needed).
+PFN_cuCtxGetId_v12000 ctx_id_getter() {
+  static PFN_cuCtxGetId_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuCtxGetId_v12000)p;
+    cudaGetLastError();
+  }
+  return fn;
+}
+
+bool current_ctx_id(unsigned long long* id) {
+  PFN_cuCtxGetId_v12000 fn = ctx_id_getter();
+  return fn != nullptr && fn(nullptr, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current device's current context.
 int scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DCP_ECUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  ScratchSlot& slot = g_scratch[dev];
+  unsigned long long id = 0;
+  const bool have_id = current_ctx_id(&id);
+  if (!(have_id && slot.keyed && slot.ptr != nullptr && slot.ctx_id == id)) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();  // not sticky: leave no error for the next call to misread
       return DCP_ECUDA;
-    g_scratch_ptr[dev] = p;
+    }
+    // the lookup may have initialised the device's context: key on it now
+    slot.ptr = p;
+    slot.keyed = current_ctx_id(&slot.ctx_id);
   }
-  *out = g_scratch_ptr[dev];
+  *out = slot.ptr;
   return DCP_OK;
 }
 

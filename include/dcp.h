@@ -294,14 +294,18 @@ int dcp_decode_gqa(dcp_layout_t layout, const void* q, int32_t num_reqs, int32_t
  * allocate device memory when they decode (a runtime that owns all device
  * memory and gives the library none, code running under a fixed memory
  * budget, or a C caller with no device allocator).  The split-KV workspace
- * comes from a fixed 16 MiB array inside the library's own device memory,
- * which every GPU that loads the library holds until the process exits.
+ * comes from a fixed 16 MiB array inside the library's own device memory.
  * Arguments and results are those of dcp_decode_gqa.
  *  - Returns DCP_EWORKSPACE, launching nothing, when the batch needs more
  *    than 16 MiB of workspace (dcp_decode_workspace_size tells in advance).
- *  - The first call on a device looks up the array's device address (once
- *    per device, with that device current); make that first call before
- *    any stream capture.
+ *  - The array is reserved on a device by the first call made there (the
+ *    library's device code loads lazily); the device then holds it until the
+ *    process exits.  That first call returns DCP_ECUDA if the 16 MiB cannot
+ *    be reserved.  Make it before any stream capture, as a warm-up.
+ *  - The array's device address is looked up with that device current and
+ *    cached with the id of the CUDA context it was found in; a call made in
+ *    another context (after cudaDeviceReset, or under a context the caller
+ *    created) looks it up again.
  *  - Every call on a device uses the same array: calls that overlap on the
  *    GPU (different streams, concurrent graphs) race and corrupt each
  *    other's results.  Calls in one stream order are safe.  The array keeps

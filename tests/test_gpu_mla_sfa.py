@@ -1,4 +1,4 @@
-"""MLA and SFA decode vs the fp64 oracle (small cases; full-size sampled)."""
+"""MLA and SFA decode vs the fp64 oracle (small cases; full size: every request)."""
 import dataclasses
 
 import numpy as np
@@ -88,18 +88,34 @@ def test_sfa_small(lib, cfg):
                 check(cfg, po[r, b, h], pl[r, b, h], po_ref[r], pl_ref[r], f"r{r} b{b} h{h}")
 
 
-def test_sfa_full_size_sampled(lib):
+def test_sfa_full_size_all_heads(lib):
+    """Every request and every head of the SFA workload: the fused output and
+    LSE (sink applied once) and every rank's partial, against the oracle."""
     wl = D.build(SFA)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, lse = lib.sfa_decode(wl.layout, wl.q, wl.kv, wl.topk, wl.seq_lens, SFA.scale, SFA.dv,
-                              sink=wl.sink)
+                              sink=wl.sink, err=err)
+    rk, sl = lib.sfa_remap(wl.layout, wl.topk, wl.seq_lens, wl.block_table, wl.num_blocks,
+                           err=err)
+    po, pl = lib.sfa_decode_partial(wl.layout, wl.q, wl.kv, rk, sl, SFA.scale, SFA.dv, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
     out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    po, pl = po.cpu().numpy(), pl.cpu().numpy()
     sink = wl.sink.cpu().numpy()
-    rng = np.random.default_rng(4)
-    for b in rng.choice(SFA.B, 4, replace=False):
-        heads = sorted(rng.choice(SFA.Hq, 3, replace=False).tolist())
-        exp = ref.sfa_expected(SFA, wl.seq_lens_host, wl.topk_host, int(b), heads, sink=sink)
+    worst = ref.WorstError()
+    heads = range(SFA.Hq)
+    for b, exp in ref.expected_for_requests(
+            lambda b: ref.sfa_expected(SFA, wl.seq_lens_host, wl.topk_host, b, heads, sink=sink),
+            range(SFA.B)):
         for h in heads:
-            ref.check_bf16(out[b, h], lse[b, h], exp[h][0], exp[h][1], f"b{b} h{h}")
+            o_ref, lse_ref, po_ref, pl_ref = exp[h]
+            ref.check_bf16(out[b, h], lse[b, h], o_ref, lse_ref, f"b{b} h{h}")
+            worst.add(out[b, h], o_ref)
+            for r in range(SFA.dcp):
+                ref.check_bf16(po[r, b, h], pl[r, b, h], po_ref[r], pl_ref[r], f"r{r} b{b} h{h}")
+                worst.add(po[r, b, h], po_ref[r], partial=True)
+    print(SFA.name, worst)
 
 
 # The fused call on shapes the small cases miss: long per-rank selections
@@ -199,7 +215,10 @@ def test_sfa_duplicate_indices_are_attended_as_listed(lib):
                 ref.check_bf16(po[r, b, h], pl[r, b, h], po_ref[r], pl_ref[r], f"r{r} b{b} h{h}")
 
 
-def mla_sampled(lib, cfg, reqs, heads_per_req, seed):
+def mla_full(lib, cfg, heads_per_req, seed):
+    """Every request, with heads_per_req seeded heads each (an fp64 check of all
+    128 heads of 6M tokens would take hours): the fused output and LSE and
+    every rank's partial, against the oracle."""
     wl = D.build(cfg)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, lse = lib.decode_mla(wl.layout, wl.q, wl.kv, wl.local_lens, cfg.scale, cfg.dv, err=err)
@@ -209,15 +228,22 @@ def mla_sampled(lib, cfg, reqs, heads_per_req, seed):
     assert err.item() == 0
     out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
     po, pl = po.cpu().numpy(), pl.cpu().numpy()
+    lens = wl.seq_lens_host
+    del wl
     rng = np.random.default_rng(seed)
-    for b in reqs:
-        heads = sorted(rng.choice(cfg.Hq, heads_per_req, replace=False).tolist())
-        exp = ref.mla_expected(cfg, wl.seq_lens_host, b, heads)
-        for h in heads:
+    heads = {b: sorted(rng.choice(cfg.Hq, heads_per_req, replace=False).tolist())
+             for b in range(cfg.B)}
+    worst = ref.WorstError()
+    for b, exp in ref.expected_for_requests(lambda b: ref.mla_expected(cfg, lens, b, heads[b]),
+                                            range(cfg.B), workers=2):
+        for h in heads[b]:
             o_ref, lse_ref, po_ref, pl_ref = exp[h]
             ref.check_bf16(out[b, h], lse[b, h], o_ref, lse_ref, f"b{b} h{h}")
+            worst.add(out[b, h], o_ref)
             for r in range(cfg.dcp):
                 ref.check_bf16(po[r, b, h], pl[r, b, h], po_ref[r], pl_ref[r], f"r{r} b{b} h{h}")
+                worst.add(po[r, b, h], po_ref[r], partial=True)
+    print(cfg.name, worst)
 
 
 def test_mla_bad_block_table_entries_are_counted(lib):
@@ -243,15 +269,12 @@ def test_mla_bad_block_table_entries_are_counted(lib):
         check(cfg, out[1, h], lse[1, h], exp[h][0], exp[h][1], f"b1 h{h}")
 
 
-def test_mla_bf16_b64_full_size_sampled(lib):
-    lens = W.make_seq_lens(MLA)
-    order = np.argsort(lens)
-    reqs = sorted({int(order[0]), int(order[-1]), int(order[len(order) // 2]), 7})
-    mla_sampled(lib, MLA, reqs, 3, seed=0)
+def test_mla_bf16_b64_full_size_all_requests(lib):
+    mla_full(lib, MLA, 4, seed=0)
 
 
-def test_longtail_mla_sampled(lib):
-    mla_sampled(lib, W.CONFIGS["longtail_mla"], [0, 1, 2, 3], 2, seed=1)
+def test_longtail_mla_full_size_all_requests(lib):
+    mla_full(lib, W.CONFIGS["longtail_mla"], 4, seed=1)
 
 
 @pytest.mark.parametrize("dcp_size", [1, 2])

@@ -30,6 +30,11 @@ def test_streams_are_deterministic_and_sliceable():
     rows = W.token_rows(cfg, W.T_K, 3, 10, 20)
     for h in range(cfg.Hkv):
         assert (W.head_rows(cfg, W.T_K, 3, h, 10, 20) == rows[:, h * 128:(h + 1) * 128]).all()
+    xs = np.array([17, 10, 19, 10])
+    assert (W.token_rows_at(cfg, W.T_K, 3, xs) == rows[xs - 10]).all()
+    sfa = W.CONFIGS["sfa_bf16_b32"]
+    lat = W.token_rows(sfa, W.T_LATENT, 1, 0, 40)
+    assert (W.token_rows_at(sfa, W.T_LATENT, 1, [39, 0, 7]) == lat[[39, 0, 7]]).all()
     other = W.stream_values(2, W.T_V, 3, 0, 5000, "bf16")
     assert (a != other).mean() > 0.9
     f = W.as_float64(W.stream_values(9, W.T_Q, 0, 0, 1 << 20, "bf16"), "bf16")

@@ -309,3 +309,18 @@ def head_rows(cfg: Config, tensor: int, b: int, h: int, x0: int, x1: int) -> np.
     for f in futs:
         f.result()
     return out
+
+
+def token_rows_at(cfg: Config, tensor: int, b: int, xs) -> np.ndarray:
+    """Rows of the tokens xs (any order, any values >= 0) of request b:
+    [len(xs), row_elems] (fp32 or bf16 bits), without generating the rest of
+    the context (the sparse top-k checks need 2048 rows of a 128k context)."""
+    table = value_table(cfg.dtype)
+    key = stream_key(cfg.seed, tensor, b)
+    w = row_elems(cfg, tensor)
+    xs = np.asarray(xs, dtype=np.int64)
+    out = np.empty((len(xs), w), dtype=table.dtype)
+    if len(xs):
+        idx = xs[:, None] * w + np.arange(w, dtype=np.int64)[None, :]
+        _fill_at(key, idx, table, out)
+    return out
