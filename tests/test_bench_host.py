@@ -58,3 +58,15 @@ def test_traffic_entries_name_a_committed_capture(name):
         assert t == e["dram_bytes"]
     else:
         assert t is None
+
+
+def test_cpu_baseline_reports_the_host_and_the_sample_share():
+    import workloads as W
+    cfg = W.CONFIGS["tiny_gqa_f32"]
+    lens = W.make_seq_lens(cfg)
+    cb = bench.cpu_baseline(cfg, lens, 0.01)
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1
+    assert cb["nproc"] == os.cpu_count() and isinstance(cb["cpu_model"], str) and cb["cpu_model"]
+    assert cb["step_kv_bytes"] == bench.step_bytes(cfg, lens, cfg.B)[0]
+    assert 0 < cb["sample_fraction_of_step"] <= 1.0
+    assert cb["sample_kv_bytes"] == round(cb["sample_fraction_of_step"] * cb["step_kv_bytes"])
