@@ -12,6 +12,7 @@ struct SfaTcArgs {
   CUtensorMap qmap;                     // q [B*Hq rows][576] bf16, box 64 x 64, 128 B swizzle
   const uint8_t* pool[DCP_MAX_RANKS];   // per-rank latent pools [num_blocks*bs rows][576] bf16
   int B, Hq, hblocks, bs, K;
+  int dcp, rpc;                         // ranks; ranks per CTA (set by launch_sfa_tc)
   float sl2;                            // softmax scale * log2(e)
   int64_t num_blocks;
   const int32_t* sel_rank;               // [B][K] remapped owner rank (-1: not selected)
@@ -29,5 +30,7 @@ bool sfa_tc_supported(int Hq, int dk, int dv, dcp_dtype_t dtype, int K, int64_t 
 // stream, which must be the dcp_sfa_remap that produced sel_rank / sel_slot
 // (the kernel reads q and sets up before waiting for it).
 int launch_sfa_tc(const SfaTcArgs& A, const void* q, int dcp, cudaStream_t s, bool pdl = false);
+// Ranks one CTA of the kernel covers for this shape (host side).
+int sfa_tc_ranks_per_cta(int dcp, int B, int hblocks);
 
 }  // namespace dcp
