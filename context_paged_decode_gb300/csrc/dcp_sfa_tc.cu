@@ -33,15 +33,22 @@
 //    head sit in one thread: tensor-memory lanes 0-15 of each lane quarter
 //    hold heads 16q .. 16q+15 (the M=64 accumulator layout), and the
 //    softmax's maximum and sum need no exchange between threads;
-//  * six warps gather with 16-byte cp.async (whole 1152-byte rows;
-//    unselected, unusable and tail rows are zero-filled): three fill slot 0
-//    and three slot 1, so two stages are in flight and a stage's barrier
-//    never waits for the other slot.  Each gather thread waits for its own
-//    copies and fences them for the tensor core before its warp arrives;
-//  * tensor memory: two S buffers (64 columns each), O^T (4 x 64 columns);
-//  * warps 0-3: softmax of their lane quarter's 16 heads (one head per
-//    thread), rescale and epilogue of their quarter of O^T (value rows).
-//    Warp 4 issues Q.K^T and warp 5 P V.  O^T columns (heads) are rescaled
+//  * five warps gather with 16-byte cp.async (whole 1152-byte rows;
+//    unselected, unusable and tail rows are zero-filled).  Each walks every
+//    stage, taking a fifth of its rows (the extra row group rotates), and
+//    never waits for its copies: cp.async.mbarrier.arrive.noinc arrives on
+//    the slot's barrier once the thread's copies have landed, so all five
+//    warps start on a slot the moment it is free.  The threads that wait on
+//    that barrier fence the data for the tensor core;
+//  * one thread issues a tcgen05.mma only every ~55-80 cycles, so Q.K^T is
+//    split between two issuing warps (latent chunks 0-4 and 5-8) into two
+//    partial accumulators that the softmax adds, in a fixed order;
+//  * tensor memory: two pairs of partial S buffers (64 columns each), O^T
+//    (4 x 64 columns);
+//  * warps 0-3: softmax of their lane quarter's 16 heads (threads l and
+//    l + 16 take tokens 0-31 and 32-63 of head 16 q + l), rescale and
+//    epilogue of their quarter of O^T (value rows).  Warps 4 and 6 issue
+//    Q.K^T, warp 5 P V.  O^T columns (heads) are rescaled
 //    only when a head's running maximum grows by more than 8 (log2 units),
 //    which keeps P <= 256; the P V warp orders that rescale between two
 //    P Vs.
@@ -82,26 +89,28 @@ constexpr int kBarOff = kMiscOff + kMiscWords * 4;
 constexpr int kNumBars = 16;
 constexpr int kSfaTcSmem = 1024 + kBarOff + kNumBars * 8 + 16;
 constexpr int kSoftmaxWarps = 4;
-constexpr int kQkWarp = 4, kPvWarp = 5;
-constexpr int kFirstGather = 6;
-constexpr int kGatherPerSlot = 3;
-constexpr int kSfaTcThreads = 32 * (kFirstGather + 2 * kGatherPerSlot);   // 384
+constexpr int kQkWarpA = 4, kPvWarp = 5, kQkWarpB = 6;
+constexpr int kQkSplit = 5;                            // chunks [0, 5) -> S_a, [5, 9) -> S_b
+constexpr int kFirstGather = 7;
+constexpr int kGatherWarps = 5;
+constexpr int kSfaTcThreads = 32 * (kFirstGather + kGatherWarps);   // 384
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 2 * kSt;
+constexpr uint32_t kColSa = 0, kColSb = 2 * kSt, kColO = 4 * kSt;
 constexpr float kRescaleThreshold = 8.f;
 constexpr int kStuck = 1 << 20;
 
 static_assert(kSfaTcSmem <= 227 * 1024, "shared memory overflow");
 static_assert(kSlotOff % 1024 == 0 && kStageB % 1024 == 0, "swizzle atoms need 1 KB alignment");
 static_assert(kColO + 4 * kHB <= kTmemCols, "tensor memory overflow");
+static_assert(kSfaTcThreads <= 384, "three warps per sub-partition keep 168 registers a thread");
 static_assert(kMaxSelTc <= 4096 && kSt < 128 && DCP_MAX_RANKS <= 32, "stage-table fields");
 
 // barrier slots
 enum : int {
   B_Q_FULL = 0,
-  B_FULL = 1,        // +slot: the stage in the slot landed (gather warps)
+  B_FULL = 1,        // +slot: the stage in the slot landed (every gather thread's copies)
   B_SLOT_FREE = 3,   // +slot: the P V that read the slot completed
-  B_S_FULL = 5,      // +buffer: S of the stage is complete
+  B_S_FULL = 5,      // +buffer: both partial S of the stage are complete
   B_S_FREE = 7,      // +buffer: the softmax warps read it
   B_P_FULL = 9,      // +stage parity: P^T, the factors and the rescale flags are stored
   B_PVD = 11,        // one phase per P V completed
@@ -112,7 +121,8 @@ enum : int {
 };
 
 __device__ __forceinline__ int arrivals(int i) {
-  if (i == B_FULL || i == B_FULL + 1) return kGatherPerSlot;
+  if (i == B_FULL || i == B_FULL + 1) return 32 * kGatherWarps;
+  if (i == B_S_FULL || i == B_S_FULL + 1) return 2;
   if (i == B_S_FREE || i == B_S_FREE + 1 || i == B_P_FULL || i == B_P_FULL + 1 ||
       i == B_RS_DONE || i == B_IX || i == B_DRAIN)
     return kSoftmaxWarps;
@@ -129,12 +139,14 @@ __device__ __forceinline__ void cp_async16_fill(uint32_t dst, const void* src, u
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the arrival is counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // One word per stage: first entry of the stage in the selection list (12
@@ -151,8 +163,8 @@ __device__ __forceinline__ bool st_last(int e) { return (e >> 25) & 1; }
 
 }  // namespace
 
-// Twelve warps put three on every SM sub-partition (16K registers each), so a
-// thread may hold up to 168 registers.
+// Twelve warps put three on every SM sub-partition (16K registers each), so
+// a thread may hold up to 168 registers.
 __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_constant__ SfaTcArgs A) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -186,7 +198,7 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
       tma_load_2d(sbase + kQOff + c * kHB * 128, &A.qmap, 64 * c, b * A.Hq + h0,
                   bars + 8 * B_Q_FULL);
   }
-  if (warp == kQkWarp) {
+  if (warp == kQkWarpA) {
     tc_alloc(smem_u32(tmem_slot), kTmemCols);
     tc_relinquish();
   }
@@ -276,13 +288,11 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
   };
 
   if (warp >= kFirstGather) {
-    // ---------------- gather: warp group `slot` fills slot n & 1 ----------------
-    // Two groups, one per slot, each with one stage in flight: a stage's
-    // barrier then never waits for the other slot to drain.
-    const int slot = (warp - kFirstGather) / kGatherPerSlot;
-    const int gw_in = (warp - kFirstGather) % kGatherPerSlot;
+    // ---------------- gather: every warp takes part in every stage ----------------
+    const int gw = warp - kFirstGather;
     bool dead = false;
-    for (int n = slot; n < nst; n += 2) {
+    for (int n = 0; n < nst; ++n) {
+      const int slot = n & 1;
       // the slot is free once the P V of stage n - 2 completed
       if (!wwait(bars + 8 * (B_SLOT_FREE + slot), ((n >> 1) & 1) ^ 1)) {
         dead = true;
@@ -296,10 +306,11 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
       // group); each copy instruction moves chunk c of the 4 rows: lane l
       // copies 16-byte unit l % 8 of row 4 g + l / 8, swizzled by the row & 7.
       // All 32 lanes copy in every instruction: the load pipe's cost is per
-      // instruction, whatever its active lanes.
+      // instruction, whatever its active lanes.  16 groups over five warps:
+      // the warp with the sixteenth group changes from stage to stage.
       const int rsub = lane >> 3, un = lane & 7;
 #pragma unroll 1
-      for (int rg = gw_in; rg < kSt / 4; rg += kGatherPerSlot) {
+      for (int rg = (gw + n) % kGatherWarps; rg < kSt / 4; rg += kGatherWarps) {
         const int rr = rg * 4 + rsub;
         const int row = rr < cnt ? sel[s0 + rr] : -1;
         const uint8_t* rsrc = row >= 0 ? pool + (int64_t)row * kRowB + un * 16 : pool;
@@ -309,15 +320,12 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
         for (int c = 0; c < kChunks; ++c)
           cp_async16_fill(rdst + c * kChunkB, row >= 0 ? rsrc + c * 128 : pool, bytes);
       }
-      cp_async_commit();
-      // the stage landed: make it visible to the tensor core
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      warp_arrive(bars + 8 * (B_FULL + slot));
+      cp_async_arrive_noinc(bars + 8 * (B_FULL + slot));
     }
+    cp_async_wait<0>();
     if (dead && lane == 0) atomicAdd(errp, kStuck);
     // ranks of the group with no selected token: o = 0, lse = -inf
-    const int zt = tid - 32 * kFirstGather, zn = 32 * 2 * kGatherPerSlot;
+    const int zt = tid - 32 * kFirstGather, zn = 32 * kGatherWarps;
     for (int j = 0; j < nr; ++j) {
       if (misc[8 + j] != 0) continue;
       const int64_t orow = ((int64_t)(r0 + j) * A.B + b) * A.Hq + h0;
@@ -325,9 +333,11 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
       for (int i = zt; i < kHB * 512 / 4; i += zn) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int i = zt; i < kHB; i += zn) A.part_lse[orow + i] = -INFINITY;
     }
-  } else if (warp == kQkWarp) {
-    // ---------------- Q.K^T issuer ----------------
+  } else if (warp == kQkWarpA || warp == kQkWarpB) {
+    // ---------------- Q.K^T issuers: chunks [c0, c1) into partial S ----------------
     if (lane == 0) {
+      const int c0 = warp == kQkWarpA ? 0 : kQkSplit, c1 = warp == kQkWarpA ? kQkSplit : kChunks;
+      const uint32_t col = warp == kQkWarpA ? kColSa : kColSb;
       bool dead = nst > 0 && !mbar_wait(bars + 8 * B_Q_FULL, 0);
       for (int n = 0; n < nst && !dead; ++n) {
         const int sb = n & 1;                                  // slot and S buffer
@@ -336,16 +346,19 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
           dead = true;
           break;
         }
+        // the gathered rows were written by cp.async (generic proxy): make
+        // them visible to the tensor core's reads
+        fence_proxy_async_smem();
         tc_fence_after();
         const uint32_t st = sbase + kSlotOff + sb * kStageB;
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
+#pragma unroll 1
+        for (int c = c0; c < c1; ++c) {
           const uint64_t ad = sdesc_sw128(sbase + kQOff + c * kHB * 128, 0, 1024);
           const uint64_t bd = sdesc_sw128(st + c * kChunkB, 0, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_ss(tmem + kColS + sb * kSt, ad + (uint64_t)((kk * 32) >> 4),
-                      bd + (uint64_t)((kk * 32) >> 4), kIdescQK, (c | kk) != 0);
+            tc_mma_ss(tmem + col + sb * kSt, ad + (uint64_t)((kk * 32) >> 4),
+                      bd + (uint64_t)((kk * 32) >> 4), kIdescQK, (c > c0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(bars + 8 * (B_S_FULL + sb));
       }
@@ -393,6 +406,7 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
           }
           ++rsc;
         }
+        fence_proxy_async_smem();
         tc_fence_after();
         // O^T[mb] += V^T . P^T: V^T is MN-major (value columns contiguous, the
         // two 64-column chunks of row block mb one chunk apart); P^T is
@@ -426,11 +440,12 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
     }
   } else {
     // ---------------- softmax, rescale, epilogue (warps 0-3, lane quarter = warp) --------
-    // Thread l < 16 of warp w owns head hl = 16 w + l: its running maximum
-    // m (log2 units) and sum l.  Every lane takes part in the rescale and the
-    // epilogue of the quarter's value rows.
-    const int hl = 16 * warp + lane;                           // valid for lane < 16
-    const bool head = lane < 16;
+    // Threads l and l + 16 of warp w own head hl = 16 w + l: tokens 0-31 and
+    // 32-63 of every stage, the running maximum m (log2 units, the same in
+    // both) and a share of the sum l.  Every lane takes part in the rescale
+    // and the epilogue of the quarter's value rows.
+    const int hl = 16 * warp + (lane & 15);
+    const bool hi = lane >= 16;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     float m2 = -INFINITY, l2 = 0.f;
     uint32_t rsc = 0, ixc = 0;
@@ -465,17 +480,26 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
         break;
       }
       tc_fence_after();
-      float s[64];
+      // S = S_a + S_b for tokens 0-31 (kept) and 32-63 (handed to lane + 16);
+      // lanes 16-31 of the quarter hold no head (M=64 layout)
+      float s[32];
       {
-        uint32_t u0[32], u1[32];
-        tc_ld32(tmem + lane_off + kColS + sb * kSt, u0);
-        tc_ld32(tmem + lane_off + kColS + sb * kSt + 32, u1);
-        tc_wait_ld(u0);
-        tc_wait_ld(u1);
+        uint32_t a0[32], b0[32];
+        tc_ld32(tmem + lane_off + kColSa + sb * kSt, a0);
+        tc_ld32(tmem + lane_off + kColSb + sb * kSt, b0);
+        tc_wait_ld(a0);
+        tc_wait_ld(b0);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(a0[i]) + __uint_as_float(b0[i]);
+        tc_ld32(tmem + lane_off + kColSa + sb * kSt + 32, a0);
+        tc_ld32(tmem + lane_off + kColSb + sb * kSt + 32, b0);
+        tc_wait_ld(a0);
+        tc_wait_ld(b0);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(u0[i]);
-          s[32 + i] = __uint_as_float(u1[i]);
+          const float up = __shfl_sync(0xffffffffu, __uint_as_float(a0[i]) + __uint_as_float(b0[i]),
+                                       lane & 15);
+          s[i] = hi ? up : s[i];
         }
       }
       tc_fence_before();
@@ -485,42 +509,42 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
           __ballot_sync(0xffffffffu, lane < cnt && sel[s0 + lane] >= 0);
       const uint32_t v_hi =
           __ballot_sync(0xffffffffu, lane + 32 < cnt && sel[s0 + lane + 32] >= 0);
+      const uint32_t vm = hi ? v_hi : v_lo;
       // this head's stage maximum (raw scores; the scale is positive)
       float mx = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < 64; ++t) {
-        const bool v = ((t < 32 ? v_lo >> t : v_hi >> (t - 32)) & 1u) != 0;
-        mx = fmaxf(mx, v ? s[t] : -INFINITY);
-      }
+      for (int t = 0; t < 32; ++t) mx = fmaxf(mx, ((vm >> t) & 1u) ? s[t] : -INFINITY);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       const float tm = mx * A.sl2;
       const bool grow = tm > m2 + kRescaleThreshold;
-      const bool need = head && grow && m2 > -INFINITY;         // O^T already holds its sums
+      const bool need = grow && m2 > -INFINITY;                 // O^T already holds its sums
       const float f = need ? exp2f(m2 - tm) : 1.f;
       if (grow) m2 = tm;
       l2 *= f;
       const uint32_t need_w = __ballot_sync(0xffffffffu, need);
-      if (head) fac[sb * kHB + hl] = f;
+      if (!hi) fac[sb * kHB + hl] = f;
       if (lane == 0) flags[sb * 4 + warp] = need_w != 0 ? 1 : 0;
-      // P (fp32 in s) and row hl of P^T in the slot's rope chunk: 64 tokens
-      // (bf16), 16-byte units swizzled by hl & 7
+      // P (fp32 in s) and this thread's half of row hl of P^T in the slot's
+      // rope chunk: 32 tokens (bf16), 16-byte units swizzled by hl & 7
       float ps = 0.f;
 #pragma unroll
-      for (int t = 0; t < 64; ++t) {
-        const bool v = ((t < 32 ? v_lo >> t : v_hi >> (t - 32)) & 1u) != 0;
-        s[t] = v ? ex2_ftz(fmaf(s[t], A.sl2, -m2)) : 0.f;
+      for (int t = 0; t < 32; ++t) {
+        s[t] = ((vm >> t) & 1u) ? ex2_ftz(fmaf(s[t], A.sl2, -m2)) : 0.f;
         ps += s[t];
       }
-      if (head) {
+      l2 += ps;
+      {
         const uint32_t prow = sbase + kSlotOff + sb * kStageB + 8 * kChunkB + hl * 128;
+        const int u0 = hi ? 4 : 0;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((u ^ (hl & 7)) << 4)),
+        for (int u = 0; u < 4; ++u)
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                           prow + (((u0 + u) ^ (hl & 7)) << 4)),
                        "r"(pack_bf16(s[8 * u], s[8 * u + 1])),
                        "r"(pack_bf16(s[8 * u + 2], s[8 * u + 3])),
                        "r"(pack_bf16(s[8 * u + 4], s[8 * u + 5])),
                        "r"(pack_bf16(s[8 * u + 6], s[8 * u + 7]))
                        : "memory");
-        l2 += ps;
       }
       fence_proxy_async_smem();
       warp_arrive(bars + 8 * (B_P_FULL + sb));
@@ -554,11 +578,12 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
           break;
         }
         ++rsc;
+        const float lt = l2 + __shfl_xor_sync(0xffffffffu, l2, 16);
         const int r = r0 + st_seg(e);
         const int64_t orow = ((int64_t)r * A.B + b) * A.Hq + h0;   // row of head h0
-        if (head) {
-          invl[hl] = l2 > 0.f ? 1.f / l2 : 0.f;
-          A.part_lse[orow + hl] = l2 > 0.f ? (m2 + log2f(l2)) * kLn2 : -INFINITY;
+        if (!hi) {
+          invl[hl] = lt > 0.f ? 1.f / lt : 0.f;
+          A.part_lse[orow + hl] = lt > 0.f ? (m2 + log2f(lt)) * kLn2 : -INFINITY;
         }
         warp_arrive(bars + 8 * B_IX);
         if (!wwait(bars + 8 * B_IX, ixc & 1)) {
@@ -592,7 +617,7 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
   if (tid == 0 && nst == 0 && !mbar_wait(bars + 8 * B_Q_FULL, 0)) atomicAdd(errp, kStuck);
   tc_fence_before();
   __syncthreads();
-  if (warp == kQkWarp) {
+  if (warp == kQkWarpA) {
     __syncwarp();
     tc_fence_after();
     tc_dealloc(tmem, kTmemCols);
