@@ -93,6 +93,7 @@ constexpr int kQkWarpA = 4, kPvWarp = 5, kQkWarpB = 6;
 constexpr int kQkSplit = 5;                            // chunks [0, 5) -> S_a, [5, 9) -> S_b
 constexpr int kFirstGather = 7;
 constexpr int kGatherWarps = 5;
+constexpr bool kL2Hints = true;   // gathered rows evict first; partials (read by the merge) last
 constexpr int kSfaTcThreads = 32 * (kFirstGather + kGatherWarps);   // 384
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColSa = 0, kColSb = 2 * kSt, kColO = 4 * kSt;
@@ -137,6 +138,22 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kHB, true, false);
 // 16 bytes global -> shared; bytes == 0 writes zeros and reads nothing.
 __device__ __forceinline__ void cp_async16_fill(uint32_t dst, const void* src, uint32_t bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
+}
+// The same with an L2 eviction policy.
+__device__ __forceinline__ void cp_async16_fill_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                                     uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+               "l"(src), "r"(bytes), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void st_f32_hint(float* dst, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(dst), "f"(v), "l"(policy)
                : "memory");
 }
 template <int N>
@@ -316,9 +333,16 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
         const uint8_t* rsrc = row >= 0 ? pool + (int64_t)row * kRowB + un * 16 : pool;
         const uint32_t bytes = row >= 0 ? 16u : 0u;
         const uint32_t rdst = dst0 + rr * 128 + ((uint32_t)(un ^ (rr & 7)) << 4);
+        if (kL2Hints) {
+          const uint64_t pol = policy_evict_first();
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c)
-          cp_async16_fill(rdst + c * kChunkB, row >= 0 ? rsrc + c * 128 : pool, bytes);
+          for (int c = 0; c < kChunks; ++c)
+            cp_async16_fill_hint(rdst + c * kChunkB, row >= 0 ? rsrc + c * 128 : pool, bytes, pol);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c)
+            cp_async16_fill(rdst + c * kChunkB, row >= 0 ? rsrc + c * 128 : pool, bytes);
+        }
       }
       cp_async_arrive_noinc(bars + 8 * (B_FULL + slot));
     }
@@ -603,9 +627,17 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
             uint32_t o[32];
             tc_ld32(tmem + lane_off + kColO + 64 * mb + 32 * hh, o);
             tc_wait_ld(o);
+            if (kL2Hints) {
+              const uint64_t pol = policy_evict_last();
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              A.part_o[(orow + 32 * hh + i) * 512 + d] = __uint_as_float(o[i]) * inv[32 * hh + i];
+              for (int i = 0; i < 32; ++i)
+                st_f32_hint(A.part_o + (orow + 32 * hh + i) * 512 + d,
+                            __uint_as_float(o[i]) * inv[32 * hh + i], pol);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                A.part_o[(orow + 32 * hh + i) * 512 + d] = __uint_as_float(o[i]) * inv[32 * hh + i];
+            }
           }
         }
         tc_fence_before();
