@@ -33,22 +33,23 @@
 //    head sit in one thread: tensor-memory lanes 0-15 of each lane quarter
 //    hold heads 16q .. 16q+15 (the M=64 accumulator layout), and the
 //    softmax's maximum and sum need no exchange between threads;
-//  * five warps gather with 16-byte cp.async (whole 1152-byte rows;
+//  * four warps gather with 16-byte cp.async (whole 1152-byte rows;
 //    unselected, unusable and tail rows are zero-filled).  Each walks every
-//    stage, taking a fifth of its rows (the extra row group rotates), and
+//    stage, taking a quarter of its rows, and
 //    never waits for its copies: cp.async.mbarrier.arrive.noinc arrives on
 //    the slot's barrier once the thread's copies have landed, so all five
 //    warps start on a slot the moment it is free.  The threads that wait on
 //    that barrier fence the data for the tensor core;
 //  * one thread issues a tcgen05.mma only every ~55-80 cycles, so Q.K^T is
 //    split between two issuing warps (latent chunks 0-4 and 5-8) into two
-//    partial accumulators that the softmax adds, in a fixed order;
+//    partial accumulators that the softmax adds, in a fixed order, and P V
+//    between two more (O^T value rows 0-255 and 256-511);
 //  * tensor memory: two pairs of partial S buffers (64 columns each), O^T
 //    (4 x 64 columns);
 //  * warps 0-3: softmax of their lane quarter's 16 heads (threads l and
 //    l + 16 take tokens 0-31 and 32-63 of head 16 q + l), rescale and
 //    epilogue of their quarter of O^T (value rows).  Warps 4 and 6 issue
-//    Q.K^T, warp 5 P V.  O^T columns (heads) are rescaled
+//    Q.K^T, warps 5 and 7 P V.  O^T columns (heads) are rescaled
 //    only when a head's running maximum grows by more than 8 (log2 units),
 //    which keeps P <= 256; the P V warp orders that rescale between two
 //    P Vs.
@@ -89,10 +90,10 @@ constexpr int kBarOff = kMiscOff + kMiscWords * 4;
 constexpr int kNumBars = 16;
 constexpr int kSfaTcSmem = 1024 + kBarOff + kNumBars * 8 + 16;
 constexpr int kSoftmaxWarps = 4;
-constexpr int kQkWarpA = 4, kPvWarp = 5, kQkWarpB = 6;
+constexpr int kQkWarpA = 4, kPvWarp = 5, kQkWarpB = 6, kPvWarpB = 7;
 constexpr int kQkSplit = 5;                            // chunks [0, 5) -> S_a, [5, 9) -> S_b
-constexpr int kFirstGather = 7;
-constexpr int kGatherWarps = 5;
+constexpr int kFirstGather = 8;
+constexpr int kGatherWarps = 4;
 constexpr bool kL2Hints = true;   // gathered rows evict first; partials (read by the merge) last
 constexpr int kSfaTcThreads = 32 * (kFirstGather + kGatherWarps);   // 384
 constexpr uint32_t kTmemCols = 512;
@@ -110,11 +111,11 @@ static_assert(kMaxSelTc <= 4096 && kSt < 128 && DCP_MAX_RANKS <= 32, "stage-tabl
 enum : int {
   B_Q_FULL = 0,
   B_FULL = 1,        // +slot: the stage in the slot landed (every gather thread's copies)
-  B_SLOT_FREE = 3,   // +slot: the P V that read the slot completed
+  B_SLOT_FREE = 3,   // +slot: both halves of the P V that read the slot completed
   B_S_FULL = 5,      // +buffer: both partial S of the stage are complete
   B_S_FREE = 7,      // +buffer: the softmax warps read it
   B_P_FULL = 9,      // +stage parity: P^T, the factors and the rescale flags are stored
-  B_PVD = 11,        // one phase per P V completed
+  B_PVD = 11,        // one phase per P V completed (both halves)
   B_RS_GO = 12,      // the P V warp: rescale now (rescale stages), or O^T is complete
   B_RS_DONE = 13,    // the softmax warps rescaled their quarters
   B_IX = 14,         // the softmax warps published 1 / l of their heads (per segment)
@@ -123,7 +124,9 @@ enum : int {
 
 __device__ __forceinline__ int arrivals(int i) {
   if (i == B_FULL || i == B_FULL + 1) return 32 * kGatherWarps;
-  if (i == B_S_FULL || i == B_S_FULL + 1) return 2;
+  if (i == B_S_FULL || i == B_S_FULL + 1 || i == B_SLOT_FREE || i == B_SLOT_FREE + 1 ||
+      i == B_PVD)
+    return 2;
   if (i == B_S_FREE || i == B_S_FREE + 1 || i == B_P_FULL || i == B_P_FULL + 1 ||
       i == B_RS_DONE || i == B_IX || i == B_DRAIN)
     return kSoftmaxWarps;
@@ -388,15 +391,19 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
       }
       if (dead) atomicAdd(errp, kStuck);
     }
-  } else if (warp == kPvWarp) {
-    // ---------------- P V issuer ----------------
+  } else if (warp == kPvWarp || warp == kPvWarpB) {
+    // ---------------- P V issuers: O^T row blocks [2 half, 2 half + 2) ----------------
+    // The first (the leader) orders the rescales and announces the end of a
+    // segment; both wait for the rescale they need before their P V.
     if (lane == 0) {
+      const bool leader = warp == kPvWarp;
+      const int mb0 = leader ? 0 : 2;
       uint32_t pvd_seen = 0, rsc = 0, drc = 0;
       bool dead = false;
-      // Observe every phase of B_PVD in order, up to the P V of stage k.  A
-      // parity wait is unambiguous only while the barrier is at most one
-      // phase past the last one observed, so the P V of stage n is issued
-      // only after that of stage n - 1 was seen to complete.
+      // Observe every phase of B_PVD in order, up to the P V of stage k (the
+      // leader only).  A parity wait is unambiguous only while the barrier is
+      // at most one phase past the last one observed, so the leader issues
+      // the P V of stage n only after that of stage n - 1 was seen to complete.
       auto pvd_upto = [&](int k) -> bool {
         while ((int)pvd_seen <= k) {
           if (!mbar_wait(bars + 8 * B_PVD, pvd_seen & 1)) return false;
@@ -416,14 +423,14 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
           }
           ++drc;
         }
-        if (!mbar_wait(bars + 8 * (B_P_FULL + sb), (n >> 1) & 1) || !pvd_upto(n - 1)) {
+        if (!mbar_wait(bars + 8 * (B_P_FULL + sb), (n >> 1) & 1) || (leader && !pvd_upto(n - 1))) {
           dead = true;
           break;
         }
         if ((flags[sb * 4 + 0] | flags[sb * 4 + 1] | flags[sb * 4 + 2] | flags[sb * 4 + 3]) != 0) {
           // rescale stage: the softmax warps multiply their O^T quarters by
-          // the stage's factors (the P V of stage n - 1 completed)
-          mbar_arrive(bars + 8 * B_RS_GO);
+          // the stage's factors once both halves of P V n - 1 completed
+          if (leader) mbar_arrive(bars + 8 * B_RS_GO);
           if (!mbar_wait(bars + 8 * B_RS_DONE, rsc & 1)) {
             dead = true;
             break;
@@ -442,7 +449,7 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
 #pragma unroll
         for (int kk = 0; kk < kSt / 16; ++kk) {
 #pragma unroll
-          for (int mb = 0; mb < 4; ++mb) {
+          for (int mb = mb0; mb < mb0 + 2; ++mb) {
             const uint64_t vd = sdesc_sw128(st + 2 * mb * kChunkB + kk * 2048, kChunkB, 1024);
             tc_mma_ss(tmem + kColO + 64 * mb, vd, pd0 + (uint64_t)((kk * 32) >> 4), kIdescPV,
                       (first && kk == 0) ? 0u : 1u);
@@ -450,9 +457,9 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
         }
         tc_commit(bars + 8 * (B_SLOT_FREE + sb));
         tc_commit(bars + 8 * B_PVD);
-        if (st_last(e)) {
-          // the segment's O^T is complete once this P V completed: release
-          // the softmax warps for the epilogue
+        if (leader && st_last(e)) {
+          // the segment's O^T is complete once both halves of this P V
+          // completed: release the softmax warps for the epilogue
           if (!pvd_upto(n)) {
             dead = true;
             break;
@@ -508,22 +515,20 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
       // lanes 16-31 of the quarter hold no head (M=64 layout)
       float s[32];
       {
-        uint32_t a0[32], b0[32];
+        uint32_t a0[32], b0[32], a1[32], b1[32];
         tc_ld32(tmem + lane_off + kColSa + sb * kSt, a0);
         tc_ld32(tmem + lane_off + kColSb + sb * kSt, b0);
+        tc_ld32(tmem + lane_off + kColSa + sb * kSt + 32, a1);
+        tc_ld32(tmem + lane_off + kColSb + sb * kSt + 32, b1);
         tc_wait_ld(a0);
         tc_wait_ld(b0);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(a0[i]) + __uint_as_float(b0[i]);
-        tc_ld32(tmem + lane_off + kColSa + sb * kSt + 32, a0);
-        tc_ld32(tmem + lane_off + kColSb + sb * kSt + 32, b0);
-        tc_wait_ld(a0);
-        tc_wait_ld(b0);
+        tc_wait_ld(a1);
+        tc_wait_ld(b1);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float up = __shfl_sync(0xffffffffu, __uint_as_float(a0[i]) + __uint_as_float(b0[i]),
+          const float up = __shfl_sync(0xffffffffu, __uint_as_float(a1[i]) + __uint_as_float(b1[i]),
                                        lane & 15);
-          s[i] = hi ? up : s[i];
+          s[i] = hi ? up : __uint_as_float(a0[i]) + __uint_as_float(b0[i]);
         }
       }
       tc_fence_before();
