@@ -118,6 +118,7 @@ int dcp_cache_write_gqa(dcp_layout_t layout, const void* k, const void* v, int64
                         int32_t num_kv_heads, int32_t head_dim, dcp_dtype_t dtype,
                         const int64_t* slot, int64_t num_blocks, dcp_rank_ptrs_t k_cache,
                         dcp_rank_ptrs_t v_cache, int32_t* err_count, dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_cache_write_gqa");
   const int es = elem_bytes(dtype);
   if (!layout_ok(layout) || es == 0 || num_tokens < 0 || num_kv_heads < 1 || head_dim < 1 ||
       num_blocks < 0)
@@ -135,6 +136,7 @@ int dcp_cache_write_gqa(dcp_layout_t layout, const void* k, const void* v, int64
 int dcp_cache_write_mla(dcp_layout_t layout, const void* kv, int64_t num_tokens, int32_t kv_dim,
                         dcp_dtype_t dtype, const int64_t* slot, int64_t num_blocks,
                         dcp_rank_ptrs_t cache, int32_t* err_count, dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_cache_write_mla");
   const int es = elem_bytes(dtype);
   if (!layout_ok(layout) || es == 0 || num_tokens < 0 || kv_dim < 1 || num_blocks < 0)
     return DCP_EINVAL;
@@ -150,6 +152,7 @@ int dcp_gather_context_mla(dcp_layout_t layout, dcp_paged_kv_t kv, int32_t num_r
                            int32_t kv_dim, dcp_dtype_t dtype, const int32_t* req_idx,
                            const int64_t* positions, int64_t num_tokens, void* out,
                            int32_t* err_count, dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_gather_context_mla");
   const int es = elem_bytes(dtype);
   if (!layout_ok(layout) || es == 0 || num_reqs < 0 || num_tokens < 0 || kv_dim < 1 ||
       kv.num_blocks < 0 || kv.max_vblocks < 0 || kv.bt_rank_stride < 0)

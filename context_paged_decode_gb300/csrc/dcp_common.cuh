@@ -7,6 +7,10 @@
 
 #include "dcp.h"
 
+#ifndef DCP_NO_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 namespace dcp {
 
 // ---------------------------------------------------------------------------
@@ -33,6 +37,20 @@ inline int launch_status() {
 }
 
 int num_sms();  // SM count of the current device (cached per device)
+
+// Host-side NVTX range around one public call: with a profiler attached the
+// call's kernels are grouped under its name; without one a push or pop costs
+// a check of a function pointer.  -DDCP_NO_NVTX compiles the ranges out.
+struct NvtxRange {
+#ifndef DCP_NO_NVTX
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+#else
+  explicit NvtxRange(const char*) {}
+#endif
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -163,6 +163,7 @@ int dcp_sfa_compact_blocks(dcp_layout_t layout, const int32_t* topk, const int32
                            int64_t max_blocks, void* out_blocks, int32_t* out_block_ids,
                            int32_t* out_counts, int64_t* out_index, void* workspace,
                            size_t workspace_bytes, int32_t* err_count, dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_sfa_compact_blocks");
   const int es = dtype == DCP_F32 ? 4 : (dtype == DCP_BF16 ? 2 : 0);
   if (!layout_ok(layout) || es == 0 || num_queries < 0 || topk_len < 0 || num_reqs < 0 ||
       kv_dim < 1 || max_blocks < 0 || kv.num_blocks < 0 || kv.max_vblocks < 0 ||

@@ -479,6 +479,7 @@ int dcp_decode_partial_gqa(dcp_layout_t layout, const void* q, int32_t num_reqs,
                            const int32_t* local_lens, float* part_o, float* part_lse,
                            void* workspace, size_t workspace_bytes, int32_t* err_count,
                            dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_decode_partial_gqa");
   if (!gqa_args_ok(layout, q, num_reqs, num_q_heads, num_kv_heads, head_dim, dtype, kv,
                    local_lens))
     return DCP_EINVAL;
@@ -506,6 +507,7 @@ int dcp_decode_gqa(dcp_layout_t layout, const void* q, int32_t num_reqs, int32_t
                    dcp_paged_kv_t kv, const int32_t* local_lens, const float* sink, void* out,
                    dcp_dtype_t out_dtype, float* out_lse, void* workspace,
                    size_t workspace_bytes, int32_t* err_count, dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_decode_gqa");
   if (!gqa_args_ok(layout, q, num_reqs, num_q_heads, num_kv_heads, head_dim, dtype, kv,
                    local_lens) ||
       (out_dtype != DCP_F32 && out_dtype != DCP_BF16))

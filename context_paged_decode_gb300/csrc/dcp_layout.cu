@@ -354,6 +354,7 @@ int dcp_version(void) { return 100; }
 
 int dcp_local_seq_lens(dcp_layout_t layout, const int32_t* seq_lens, int32_t num_reqs,
                        int32_t* local_lens, int32_t* err_count, dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_local_seq_lens");
   if (!layout_ok(layout) || num_reqs < 0) return DCP_EINVAL;
   if (num_reqs == 0) return DCP_OK;
   if (!seq_lens || !local_lens) return DCP_EINVAL;
@@ -369,6 +370,7 @@ int dcp_slot_mapping(dcp_layout_t layout, const int32_t* req_idx, const int64_t*
                      int32_t max_vblocks, int64_t bt_rank_stride, int64_t num_blocks,
                      int32_t* out_rank, int64_t* out_slot, int32_t* err_count,
                      dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_slot_mapping");
   if (!layout_ok(layout) || num_tokens < 0 || num_reqs < 0 || max_vblocks < 0 ||
       bt_rank_stride < 0 || num_blocks < 0)
     return DCP_EINVAL;
@@ -388,6 +390,7 @@ int dcp_sfa_remap(dcp_layout_t layout, const int32_t* topk, int32_t num_reqs, in
                   const int32_t* seq_lens, const int32_t* block_table, int32_t max_vblocks,
                   int64_t bt_rank_stride, int64_t num_blocks, int32_t* out_rank,
                   int32_t* out_slot, int32_t* err_count, dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_sfa_remap");
   if (!layout_ok(layout) || num_reqs < 0 || topk_len < 0 || max_vblocks < 0 ||
       bt_rank_stride < 0 || num_blocks < 0)
     return DCP_EINVAL;

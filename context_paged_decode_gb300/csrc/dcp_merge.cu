@@ -513,6 +513,7 @@ extern "C" int dcp_lse_merge(int32_t num_parts, const float* part_o, const float
                              int32_t num_reqs, int32_t num_heads, int32_t head_dim_v,
                              const float* sink, void* out, dcp_dtype_t out_dtype, float* out_lse,
                              dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_lse_merge");
   if (num_parts < 0 || num_reqs < 0 || num_heads < 0 || head_dim_v < 4 || head_dim_v % 4 != 0 ||
       head_dim_v > 1024 || (out_dtype != DCP_F32 && out_dtype != DCP_BF16))
     return DCP_EINVAL;
@@ -528,6 +529,7 @@ extern "C" int dcp_lse_merge_swa(int32_t num_parts, const float* part_o, const f
                                  int32_t num_heads, int32_t head_dim_v, const float* sink,
                                  void* out, dcp_dtype_t out_dtype, float* out_lse,
                                  dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_lse_merge_swa");
   if (num_parts < 0 || num_reqs < 0 || num_heads < 0 || head_dim_v < 4 || head_dim_v % 4 != 0 ||
       head_dim_v > 1024 || (out_dtype != DCP_F32 && out_dtype != DCP_BF16))
     return DCP_EINVAL;

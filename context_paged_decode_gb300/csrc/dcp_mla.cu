@@ -88,6 +88,7 @@ int dcp_decode_partial_mla(dcp_layout_t layout, const void* q, int32_t num_reqs,
                            dcp_dtype_t dtype, dcp_paged_kv_t kv, const int32_t* local_lens,
                            float* part_o, float* part_lse, void* workspace,
                            size_t workspace_bytes, int32_t* err_count, dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_decode_partial_mla");
   if (!mla_args_ok(layout, q, num_reqs, num_q_heads, kv_dim, v_dim, dtype, kv, local_lens))
     return DCP_EINVAL;
   if (num_reqs == 0) return DCP_OK;
@@ -111,6 +112,7 @@ int dcp_decode_mla(dcp_layout_t layout, const void* q, int32_t num_reqs, int32_t
                    dcp_paged_kv_t kv, const int32_t* local_lens, const float* sink, void* out,
                    dcp_dtype_t out_dtype, float* out_lse, void* workspace,
                    size_t workspace_bytes, int32_t* err_count, dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_decode_mla");
   if (!mla_args_ok(layout, q, num_reqs, num_q_heads, kv_dim, v_dim, dtype, kv, local_lens) ||
       (out_dtype != DCP_F32 && out_dtype != DCP_BF16))
     return DCP_EINVAL;

@@ -93,6 +93,7 @@ extern "C" int dcp_decode_gqa_noalloc(dcp_layout_t layout, const void* q, int32_
                                       dcp_paged_kv_t kv, const int32_t* local_lens,
                                       const float* sink, void* out, dcp_dtype_t out_dtype,
                                       float* out_lse, int32_t* err_count, dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_decode_gqa_noalloc");
   size_t need = 0;
   const int rc = dcp_decode_workspace_size(layout, DCP_KIND_GQA, num_reqs, num_q_heads,
                                            num_kv_heads, head_dim, &need);

@@ -119,6 +119,7 @@ int dcp_sfa_decode_partial(dcp_layout_t layout, const void* q, int32_t num_reqs,
                            dcp_dtype_t dtype, dcp_paged_kv_t kv, const int32_t* sel_rank,
                            const int32_t* sel_slot, int32_t topk_len, float* part_o,
                            float* part_lse, int32_t* err_count, dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_sfa_decode_partial");
   if (!sfa_args_ok(layout, q, num_reqs, num_q_heads, kv_dim, v_dim, dtype, kv, topk_len))
     return DCP_EINVAL;
   if (num_reqs == 0) return DCP_OK;
@@ -150,6 +151,7 @@ int dcp_sfa_decode(dcp_layout_t layout, const void* q, int32_t num_reqs, int32_t
                    const int32_t* seq_lens, const float* sink, void* out,
                    dcp_dtype_t out_dtype, float* out_lse, void* workspace,
                    size_t workspace_bytes, int32_t* err_count, dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_sfa_decode");
   if (!sfa_args_ok(layout, q, num_reqs, num_q_heads, kv_dim, v_dim, dtype, kv, topk_len) ||
       (out_dtype != DCP_F32 && out_dtype != DCP_BF16) || kv.max_vblocks < 0 ||
       kv.bt_rank_stride < 0)

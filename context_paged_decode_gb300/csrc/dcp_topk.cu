@@ -177,6 +177,7 @@ int dcp_topk_workspace_size(dcp_layout_t layout, int32_t num_reqs, int32_t k, si
 int dcp_topk_local(dcp_layout_t layout, const float* local_scores, int32_t num_reqs,
                    int32_t max_local, const int32_t* local_lens, int32_t k, uint64_t* cand_keys,
                    dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_topk_local");
   if (!layout_ok(layout) || num_reqs < 0 || max_local < 0 || k < 1 || k > kTopkMax)
     return DCP_EINVAL;
   if (num_reqs == 0) return DCP_OK;
@@ -190,6 +191,7 @@ int dcp_topk_local(dcp_layout_t layout, const float* local_scores, int32_t num_r
 int dcp_topk_merge(int32_t dcp_size, const uint64_t* cand_keys, int32_t num_reqs, int32_t k,
                    void* workspace, size_t workspace_bytes, int32_t* out_ids, float* out_scores,
                    dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_topk_merge");
   if (dcp_size < 1 || dcp_size > DCP_MAX_RANKS || num_reqs < 0 || k < 1 || k > kTopkMax)
     return DCP_EINVAL;
   if (num_reqs == 0) return DCP_OK;
@@ -204,6 +206,7 @@ int dcp_topk_merge(int32_t dcp_size, const uint64_t* cand_keys, int32_t num_reqs
 int dcp_topk(dcp_layout_t layout, const float* local_scores, int32_t num_reqs, int32_t max_local,
              const int32_t* local_lens, int32_t k, int32_t* out_ids, float* out_scores,
              void* workspace, size_t workspace_bytes, dcp_stream_t stream) {
+  dcp::NvtxRange nvtx_range("dcp_topk");
   size_t need = 0;
   const int rc0 = dcp_topk_workspace_size(layout, num_reqs, k, &need);
   if (rc0) return rc0;
