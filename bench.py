@@ -395,8 +395,6 @@ def measure(cfg, args, world, dev, local_rank, with_e2e=True):
 
     # the dominant call alone: per-launch durations of the decode call
     dec_ms = [timed(decode, 1) for _ in range(args.steps)]
-    clk.end()
-    clocks = clk.stop()
 
     e2e_ms = None
     h2d = in_buf.numel()
@@ -431,6 +429,9 @@ def measure(cfg, args, world, dev, local_rank, with_e2e=True):
         e2e_ms = timed(run_e2e, args.steps)
         torch.cuda.synchronize()
         barrier()
+    # the clock record spans the step, decode-call and end-to-end timings
+    clk.end()
+    clocks = clk.stop()
 
     step_ms, e2e_ms_all, dec_avg = max_over_ranks(
         [step_ms, e2e_ms if e2e_ms is not None else 0.0, statistics.mean(dec_ms)],
