@@ -10,19 +10,10 @@
 #include <utility>
 
 #include "dcp_common.cuh"
+#include "dcp_merge.cuh"
 #include "dcp_ptx.cuh"
 
 namespace dcp {
-
-struct DenseParts {  // part_o [n][B][H][dv], part_lse [n][B][H]
-  const float* o;
-  const float* lse;
-  int64_t stride;  // B*H
-  __device__ __forceinline__ float lse_at(int i, int64_t row) const { return lse[i * stride + row]; }
-  __device__ __forceinline__ const float* o_at(int i, int64_t row, int dv) const {
-    return o + (i * stride + row) * dv;
-  }
-};
 
 struct DensePlusOne {  // n dense parts [n][B][H][dv] and one more part [B][H][dv]
   const float* o;
@@ -37,6 +28,7 @@ struct DensePlusOne {  // n dense parts [n][B][H][dv] and one more part [B][H][d
   __device__ __forceinline__ const float* o_at(int i, int64_t row, int dv) const {
     return i < n ? o + (i * stride + row) * dv : xo + row * dv;
   }
+  __device__ __forceinline__ float4 load4(const float4* p) const { return __ldg(p); }
 };
 
 struct ItemParts {  // plan items: lse [item][G], o [item][G][dv]
@@ -279,64 +271,6 @@ __global__ void dense_plus_one_merge_kernel(int n, const float* __restrict__ po,
   DensePlusOne P{po, pl, (int64_t)B * H, n, xo, xl};
   merge_row<CH>(P, n + 1, row, dv, sink != nullptr, sink ? sink[h] : 0.f, out, out_dtype, row,
                 out_lse);
-}
-
-// The same merge with one warp per (output row, 128-value chunk), for calls
-// with at most NP parts: every part's LSE and its 128 values are loaded
-// before any is used, so a warp waits for memory once, and there are four
-// warps per 512-wide row to hide that wait.  The arithmetic and its order are
-// those of merge_row, so the output is bitwise the same.
-template <int NP, class Parts>
-__device__ __forceinline__ void merge_chunk(const Parts& P, int n, int64_t row, int dv, int chunk,
-                                            bool has_sink, float sink, void* out, int out_dtype,
-                                            int64_t out_row, float* out_lse) {
-  const int lane = threadIdx.x & 31;
-  const int nv = dv >> 2;
-  const int idx = chunk * 32 + lane;                 // float4 of the row
-  const bool act = idx < nv;
-  const float l_mine = lane < n ? P.lse_at(lane, row) : -INFINITY;
-  float4 v[NP];
-#pragma unroll
-  for (int i = 0; i < NP; ++i)
-    v[i] = (i < n && act) ? __ldg(reinterpret_cast<const float4*>(P.o_at(i, row, dv)) + idx)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-  float m = has_sink ? sink : -INFINITY;
-  m = fmaxf(m, l_mine);
-  m = warp_max(m);
-  if (m == -INFINITY) {  // nothing attended and no sink
-    if (act) {
-      if (out_dtype == DCP_F32)
-        reinterpret_cast<float4*>(out)[out_row * nv + idx] = make_float4(0.f, 0.f, 0.f, 0.f);
-      else
-        reinterpret_cast<uint2*>(out)[out_row * nv + idx] = make_uint2(0u, 0u);
-    }
-    if (out_lse && chunk == 0 && lane == 0) out_lse[out_row] = -INFINITY;
-    return;
-  }
-  float s = l_mine != -INFINITY ? expf(l_mine - m) : 0.f;
-  s = warp_sum(s);
-  if (has_sink) s += expf(sink - m);
-  const float lse = m + logf(s);
-  const float wl = l_mine == -INFINITY ? 0.f : expf(l_mine - lse);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int i = 0; i < NP; ++i) {
-    const float w = __shfl_sync(0xffffffffu, wl, i);
-    if (i < n && w != 0.f) {  // an empty part adds nothing, whatever its o holds
-      acc.x = fmaf(w, v[i].x, acc.x);
-      acc.y = fmaf(w, v[i].y, acc.y);
-      acc.z = fmaf(w, v[i].z, acc.z);
-      acc.w = fmaf(w, v[i].w, acc.w);
-    }
-  }
-  if (act) {
-    if (out_dtype == DCP_F32)
-      reinterpret_cast<float4*>(out)[out_row * nv + idx] = acc;
-    else
-      reinterpret_cast<uint2*>(out)[out_row * nv + idx] =
-          make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
-  }
-  if (out_lse && chunk == 0 && lane == 0) out_lse[out_row] = lse;
 }
 
 template <int NP>

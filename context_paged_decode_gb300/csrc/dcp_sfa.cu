@@ -187,8 +187,10 @@ int dcp_sfa_decode(dcp_layout_t layout, const void* q, int32_t num_reqs, int32_t
     // With no top-k entries the remap launches nothing, and the partials
     // kernel must not overlap whatever the caller ran last.
     const bool after_remap = (int64_t)num_reqs * topk_len > 0;
-    rc = launch_sfa_tc(T, q, layout.dcp_size, s, after_remap);
-    if (rc) return rc;
+    bool merged = false;
+    rc = launch_sfa_tc_merged(T, q, layout.dcp_size, s, after_remap, sink, out, (int)out_dtype,
+                              out_lse, &merged);
+    if (rc || merged) return rc;
     return launch_dense_merge(dcp, part_o, part_lse, num_reqs, num_q_heads, v_dim, sink, out,
                               (int)out_dtype, out_lse, s, true);
   } else if (sfa_fast_ok(layout, q, num_q_heads, kv_dim, v_dim, dtype, kv, topk_len)) {

@@ -46,6 +46,11 @@
 //    between two more (O^T value rows 0-255 and 256-511);
 //  * tensor memory: two pairs of partial S buffers (64 columns each), O^T
 //    (4 x 64 columns);
+//  * in the fused decode the CTAs of a (request, head block) form a cluster:
+//    once each has written its ranks' partials (and a cluster barrier made
+//    them visible), each merges its share of the request's (head, 128-value
+//    chunk) rows by LSE from L2, with the sink applied once, so no separate
+//    merge launch waits for the whole grid;
 //  * warps 0-3: softmax of their lane quarter's 16 heads (threads l and
 //    l + 16 take tokens 0-31 and 32-63 of head 16 q + l), rescale and
 //    epilogue of their quarter of O^T (value rows).  Warps 4 and 6 issue
@@ -58,6 +63,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include "dcp_merge.cuh"
 #include "dcp_sfa_tc.cuh"
 
 namespace dcp {
@@ -198,10 +204,13 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
   volatile int32_t* flags = reinterpret_cast<volatile int32_t*>(smem + kFlagOff);
   float* invl = reinterpret_cast<float*>(smem + kInvOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // block -> (group of ranks, request, head block); in a fused launch the
+  // groups of one (request, head block) are consecutive blocks (one cluster)
   const int per_group = A.B * A.hblocks;
-  const int r0 = (blockIdx.x / per_group) * A.rpc;           // first rank of the group
+  const int grp = A.fuse ? (int)(blockIdx.x % A.ngroups) : (int)(blockIdx.x / per_group);
+  const int rem = A.fuse ? (int)(blockIdx.x / A.ngroups) : (int)(blockIdx.x % per_group);
+  const int r0 = grp * A.rpc;                                 // first rank of the group
   const int nr = min(A.rpc, A.dcp - r0);                      // ranks in the group
-  const int rem = blockIdx.x % per_group;
   const int b = rem / A.hblocks, h0 = (rem % A.hblocks) * kHB;
   const int64_t num_slots = A.num_blocks * A.bs;
   int32_t* errp = A.err;
@@ -659,6 +668,32 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
     tc_fence_after();
     tc_dealloc(tmem, kTmemCols);
   }
+  if (A.fuse) {
+    // every CTA of the cluster wrote its ranks' partials (release / acquire
+    // at cluster scope); CTA grp merges (head, chunk) rows grp, grp + ngroups, ...
+    cluster_sync();
+    DensePartsL2 P;
+    P.o = A.part_o;
+    P.lse = A.part_lse;
+    P.stride = (int64_t)A.B * A.Hq;
+    if (A.dcp <= 8) {
+      // one warp per head row (all four 128-value chunks): head rows grp,
+      // grp + ngroups, ...
+      for (int hh = grp + A.ngroups * warp; hh < kHB; hh += A.ngroups * (kSfaTcThreads / 32)) {
+        const int64_t row = (int64_t)b * A.Hq + h0 + hh;
+        merge_row_chunks<8, 4>(P, A.dcp, row, A.sink != nullptr, A.sink ? A.sink[h0 + hh] : 0.f,
+                               A.out, A.out_dtype, row, A.out_lse);
+      }
+    } else {
+      constexpr int kTasks = kHB * 4;                         // (head, 128-value chunk) rows
+      for (int t = grp + A.ngroups * warp; t < kTasks; t += A.ngroups * (kSfaTcThreads / 32)) {
+        const int hh = t >> 2, ch = t & 3;
+        const int64_t row = (int64_t)b * A.Hq + h0 + hh;
+        merge_chunk<16>(P, A.dcp, row, 512, ch, A.sink != nullptr, A.sink ? A.sink[h0 + hh] : 0.f,
+                        A.out, A.out_dtype, row, A.out_lse);
+      }
+    }
+  }
 }
 
 namespace {
@@ -697,11 +732,23 @@ int sfa_tc_ranks_per_cta(int dcp, int B, int hblocks) {
   return dcp;
 }
 
-int launch_sfa_tc(const SfaTcArgs& A0, const void* q, int dcp, cudaStream_t s, bool pdl) {
+namespace {
+
+int launch_sfa_tc_impl(const SfaTcArgs& A0, const void* q, int dcp, cudaStream_t s, bool pdl,
+                       bool want_merge, const float* sink, void* out, int out_dtype,
+                       float* out_lse, bool* merged) {
   SfaTcArgs A = A0;
   A.hblocks = A.Hq / kHB;
   A.dcp = dcp;
   A.rpc = sfa_tc_ranks_per_cta(dcp, A.B, A.hblocks);
+  A.ngroups = (dcp + A.rpc - 1) / A.rpc;
+  // a cluster of the ngroups CTAs of a request (portable size) merges in the kernel
+  A.fuse = want_merge && A.ngroups <= 8 ? 1 : 0;
+  A.sink = sink;
+  A.out = out;
+  A.out_dtype = out_dtype;
+  A.out_lse = out_lse;
+  if (merged) *merged = A.fuse != 0;
   if (!encode_q(&A.qmap, q, (uint64_t)A.B * A.Hq)) return DCP_ECUDA;
   static bool attr_done[64] = {false};
   int dev = 0;
@@ -715,21 +762,41 @@ int launch_sfa_tc(const SfaTcArgs& A0, const void* q, int dcp, cudaStream_t s, b
     }
     attr_done[dev] = true;
   }
-  const int grid = ((dcp + A.rpc - 1) / A.rpc) * A.B * A.hblocks;
+  const int grid = A.ngroups * A.B * A.hblocks;
   if (grid <= 0) return DCP_OK;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kSfaTcThreads);
   cfg.dynamicSmemBytes = kSfaTcSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  int na = 1;
+  if (A.fuse) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)A.ngroups;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    na = 2;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = na;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, sfa_tc_kernel, A);
   if (e != cudaSuccess) return launch_status_report(e);
   return launch_status();
+}
+
+}  // namespace
+
+int launch_sfa_tc(const SfaTcArgs& A, const void* q, int dcp, cudaStream_t s, bool pdl) {
+  return launch_sfa_tc_impl(A, q, dcp, s, pdl, false, nullptr, nullptr, 0, nullptr, nullptr);
+}
+
+int launch_sfa_tc_merged(const SfaTcArgs& A, const void* q, int dcp, cudaStream_t s, bool pdl,
+                         const float* sink, void* out, int out_dtype, float* out_lse,
+                         bool* merged) {
+  return launch_sfa_tc_impl(A, q, dcp, s, pdl, true, sink, out, out_dtype, out_lse, merged);
 }
 
 }  // namespace dcp

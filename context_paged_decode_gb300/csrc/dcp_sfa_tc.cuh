@@ -20,6 +20,14 @@ struct SfaTcArgs {
   float* part_o;                        // [dcp][B][Hq][512]
   float* part_lse;                      // [dcp][B][Hq]
   int32_t* err;
+  // merge inside the kernel (set by launch_sfa_tc): the ngroups CTAs of a
+  // (request, head block) form a cluster, and after every one has written
+  // its ranks' partials each merges its share of the rows into out / out_lse
+  int fuse, ngroups;
+  const float* sink;                    // [Hq] or null
+  void* out;                            // [B][Hq][512] of out_dtype
+  int out_dtype;
+  float* out_lse;                       // [B][Hq] or null
 };
 
 // bf16, 576-wide latent rows with a 512-wide value, Hq a multiple of 64,
@@ -30,6 +38,12 @@ bool sfa_tc_supported(int Hq, int dk, int dv, dcp_dtype_t dtype, int K, int64_t 
 // stream, which must be the dcp_sfa_remap that produced sel_rank / sel_slot
 // (the kernel reads q and sets up before waiting for it).
 int launch_sfa_tc(const SfaTcArgs& A, const void* q, int dcp, cudaStream_t s, bool pdl = false);
+// The same, merging the partials inside the kernel into out / out_lse with the
+// sink applied once when the shape allows (a cluster of the CTAs of a request:
+// at most 8 of them); *merged tells whether it did (otherwise the caller
+// merges the partials).
+int launch_sfa_tc_merged(const SfaTcArgs& A, const void* q, int dcp, cudaStream_t s, bool pdl,
+                         const float* sink, void* out, int out_dtype, float* out_lse, bool* merged);
 // Ranks one CTA of the kernel covers for this shape (host side).
 int sfa_tc_ranks_per_cta(int dcp, int B, int hblocks);
 
