@@ -5,6 +5,7 @@
 // local slots, and non-owners are masked.  The slot of each token on each
 // rank comes from dcp_slot_mapping (-1 on non-owners).
 #include "dcp_common.cuh"
+#include "dcp_ptx.cuh"
 
 namespace dcp {
 
@@ -15,6 +16,8 @@ __global__ void cache_write_kernel(const uint4* __restrict__ src0, const uint4* 
                                    int64_t T, int H, int chunks_per_row, int bs, int dcp,
                                    const int64_t* __restrict__ slot, int64_t num_slots,
                                    dcp_rank_ptrs_t dst0, dcp_rank_ptrs_t dst1, int32_t* err) {
+  griddep_launch_dependents();   // the next call's first kernel may start its launch
+  griddep_wait();                // launched chained: the preceding kernel completed
   const int64_t per_tok = (int64_t)H * chunks_per_row;
   const int64_t n = T * per_tok;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
@@ -55,12 +58,14 @@ static int launch_cache_write(int nsrc, const void* s0, const void* s1, int64_t 
   const int64_t blocks = (n + 255) / 256;
   const int grid = (int)(blocks < 16 * num_sms() ? blocks : 16 * num_sms());
   const int64_t num_slots = num_blocks * bs;
-  if (nsrc == 2)
-    cache_write_kernel<2><<<grid, 256, 0, st>>>((const uint4*)s0, (const uint4*)s1, T, H, cpr, bs,
-                                                dcp, slot, num_slots, d0, d1, err);
-  else
-    cache_write_kernel<1><<<grid, 256, 0, st>>>((const uint4*)s0, nullptr, T, H, cpr, bs, dcp,
-                                                slot, num_slots, d0, d0, err);
+  const uint4* u0 = (const uint4*)s0;
+  const uint4* u1 = nsrc == 2 ? (const uint4*)s1 : nullptr;
+  const cudaError_t e =
+      nsrc == 2 ? launch_chained(cache_write_kernel<2>, (unsigned)grid, 256, 0, st, u0, u1, T, H,
+                                 cpr, bs, dcp, slot, num_slots, d0, d1, err)
+                : launch_chained(cache_write_kernel<1>, (unsigned)grid, 256, 0, st, u0, u1, T, H,
+                                 cpr, bs, dcp, slot, num_slots, d0, d0, err);
+  if (e != cudaSuccess) return launch_status_report(e);
   return launch_status();
 }
 

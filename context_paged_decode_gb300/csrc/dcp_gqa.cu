@@ -95,6 +95,7 @@ __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16* p) {
 template <int NW, int D, bool kUpper>
 __global__ void __launch_bounds__(NW * 32)
 gqa_tma_kernel(const __grid_constant__ GqaTmaArgs A, Plan plan) {
+  griddep_launch_dependents();   // the next call's first kernel may start its launch
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ int s_item;

@@ -36,6 +36,8 @@ int num_sms() {
 // local_lens[b][r]: closed form of the number of tokens x < L with rank(x) == r.
 __global__ void local_seq_lens_kernel(Layout L, const int32_t* __restrict__ seq_lens, int B,
                                       int32_t* __restrict__ out, int32_t* err) {
+  griddep_launch_dependents();   // the next call's first kernel may start its launch
+  griddep_wait();                // launched chained: the preceding kernel completed
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= B * L.dcp) return;
   const int b = i / L.dcp, r = i % L.dcp;
@@ -60,6 +62,8 @@ __global__ void slot_mapping_kernel(Layout L, const int32_t* __restrict__ req,
                                     int64_t bt_rank_stride, int64_t num_blocks,
                                     int32_t* __restrict__ out_rank, int64_t* __restrict__ out_slot,
                                     int32_t* err) {
+  griddep_launch_dependents();
+  griddep_wait();
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < T;
        t += (int64_t)gridDim.x * blockDim.x) {
     const int b = req[t];
@@ -91,6 +95,7 @@ __global__ void sfa_remap_kernel(Layout L, const int32_t* __restrict__ topk, int
                                  int32_t* __restrict__ out_rank, int32_t* __restrict__ out_slot,
                                  int32_t* err) {
   griddep_launch_dependents();   // a dependent sparse-attention launch may start its prologue
+  griddep_wait();                // launched chained: the preceding kernel completed
   const int64_t n = (int64_t)B * K;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -169,6 +174,8 @@ __device__ __forceinline__ int block_scan_excl(int v, int* sh, int* total) {
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t* __restrict__ local_lens, int B, int dcp, int G, int tile,
             int min_chunk, int target_items, Plan plan) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ int64_t sh64[33];
   __shared__ int sh[32];
   const int n = B * G * dcp;  // entries (b, g, r)
@@ -214,8 +221,9 @@ plan_kernel(const int32_t* __restrict__ local_lens, int B, int dcp, int G, int t
 
 int launch_plan(const int32_t* local_lens, int B, int dcp, int G, int tile, int min_chunk,
                 int target_items, const Plan& plan, cudaStream_t s) {
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(local_lens, B, dcp, G, tile, min_chunk, target_items,
-                                         plan);
+  const cudaError_t e = launch_chained(plan_kernel, 1, kPlanThreads, 0, s, local_lens, B, dcp, G,
+                                       tile, min_chunk, target_items, plan);
+  if (e != cudaSuccess) return launch_status_report(e);
   return launch_status();
 }
 
@@ -254,6 +262,8 @@ __device__ __forceinline__ int64_t block_scan_excl_i64(int64_t v, int64_t* sh, i
 __global__ void __launch_bounds__(kPlanThreads)
 plan_parts_kernel(const int32_t* __restrict__ local_lens, int B, int dcp, int tile, int parts,
                   int overhead, Plan plan) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ int64_t sh64[33];
   __shared__ int sh[32];
   const int n = B * dcp;
@@ -329,7 +339,9 @@ plan_parts_kernel(const int32_t* __restrict__ local_lens, int B, int dcp, int ti
 int launch_plan_parts(const int32_t* local_lens, int B, int dcp, int tile, int parts,
                       int overhead, const Plan& plan, cudaStream_t s) {
   if (parts < 1 || parts > kMaxParts || tile < 1 || overhead < 0) return DCP_EINVAL;
-  plan_parts_kernel<<<1, kPlanThreads, 0, s>>>(local_lens, B, dcp, tile, parts, overhead, plan);
+  const cudaError_t e = launch_chained(plan_parts_kernel, 1, kPlanThreads, 0, s, local_lens, B, dcp,
+                                       tile, parts, overhead, plan);
+  if (e != cudaSuccess) return launch_status_report(e);
   return launch_status();
 }
 
@@ -360,8 +372,10 @@ int dcp_local_seq_lens(dcp_layout_t layout, const int32_t* seq_lens, int32_t num
   if (!seq_lens || !local_lens) return DCP_EINVAL;
   const Layout L{layout.dcp_size, layout.block_size, layout.interleave};
   const int n = num_reqs * layout.dcp_size;
-  local_seq_lens_kernel<<<(n + 255) / 256, 256, 0, (cudaStream_t)stream>>>(L, seq_lens, num_reqs,
-                                                                          local_lens, err_count);
+  const cudaError_t e = launch_chained(local_seq_lens_kernel, (unsigned)((n + 255) / 256), 256, 0,
+                                       (cudaStream_t)stream, L, seq_lens, num_reqs, local_lens,
+                                       err_count);
+  if (e != cudaSuccess) return launch_status_report(e);
   return launch_status();
 }
 
@@ -380,9 +394,11 @@ int dcp_slot_mapping(dcp_layout_t layout, const int32_t* req_idx, const int64_t*
   const Layout L{layout.dcp_size, layout.block_size, layout.interleave};
   const int64_t blocks = (num_tokens + 255) / 256;
   const int grid = (int)(blocks < 8 * num_sms() ? blocks : 8 * num_sms());
-  slot_mapping_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(
-      L, req_idx, positions, num_tokens, block_table, num_reqs, max_vblocks, bt_rank_stride,
-      num_blocks, out_rank, out_slot, err_count);
+  const cudaError_t e = launch_chained(slot_mapping_kernel, (unsigned)grid, 256, 0,
+                                       (cudaStream_t)stream, L, req_idx, positions, num_tokens,
+                                       block_table, num_reqs, max_vblocks, bt_rank_stride,
+                                       num_blocks, out_rank, out_slot, err_count);
+  if (e != cudaSuccess) return launch_status_report(e);
   return launch_status();
 }
 
@@ -401,10 +417,11 @@ int dcp_sfa_remap(dcp_layout_t layout, const int32_t* topk, int32_t num_reqs, in
   const Layout L{layout.dcp_size, layout.block_size, layout.interleave};
   const int64_t blocks = (n + 255) / 256;
   const int grid = (int)(blocks < 8 * num_sms() ? blocks : 8 * num_sms());
-  sfa_remap_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(L, topk, num_reqs, topk_len, seq_lens,
-                                                          block_table, max_vblocks, bt_rank_stride,
-                                                          num_blocks, out_rank, out_slot,
-                                                          err_count);
+  const cudaError_t e = launch_chained(sfa_remap_kernel, (unsigned)grid, 256, 0, (cudaStream_t)stream,
+                                       L, topk, num_reqs, topk_len, seq_lens, block_table,
+                                       max_vblocks, bt_rank_stride, num_blocks, out_rank, out_slot,
+                                       err_count);
+  if (e != cudaSuccess) return launch_status_report(e);
   return launch_status();
 }
 

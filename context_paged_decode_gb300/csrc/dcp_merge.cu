@@ -249,6 +249,7 @@ __global__ void dense_merge_kernel(int n, const float* __restrict__ po,
                                    const float* __restrict__ pl, int B, int H, int dv,
                                    const float* __restrict__ sink, void* out, int out_dtype,
                                    float* out_lse) {
+  griddep_launch_dependents();   // the next call's first kernel may start its launch
   griddep_wait();   // launched as a dependent: the partials are complete past this point
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= (int64_t)B * H) return;
@@ -278,6 +279,7 @@ __global__ void dense_merge_chunk_kernel(int n, const float* __restrict__ po,
                                          const float* __restrict__ pl, int B, int H, int dv,
                                          int chunks, const float* __restrict__ sink, void* out,
                                          int out_dtype, float* out_lse) {
+  griddep_launch_dependents();   // the next call's first kernel may start its launch
   griddep_wait();   // launched as a dependent: the partials are complete past this point
   const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t row = wid / chunks;
@@ -313,6 +315,7 @@ template <int CH>
 __global__ void item_merge_kernel(Plan plan, int mode, int B, int dcp, int Hq, int G, int groups,
                                   int dv, const float* __restrict__ sink, void* out,
                                   int out_dtype, float* out_lse) {
+  griddep_launch_dependents();   // the next call's first kernel may start its launch
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t nrows = (int64_t)(mode == 0 ? 1 : dcp) * B * Hq;
   if (row >= nrows) return;
@@ -334,6 +337,7 @@ template <int CH>
 __global__ void __launch_bounds__(kWideWarps * 32)
 item_merge_wide_kernel(Plan plan, int mode, int B, int dcp, int Hq, int G, int groups, int dv,
                        const float* __restrict__ sink, void* out, int out_dtype, float* out_lse) {
+  griddep_launch_dependents();   // the next call's first kernel may start its launch
   const int64_t row = blockIdx.x;
   const int h = (int)(row % Hq);
   const int b = (int)((row / Hq) % B);

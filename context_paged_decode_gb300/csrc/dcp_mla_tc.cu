@@ -164,6 +164,7 @@ __device__ __forceinline__ int arrivals(int i) {
 // thread may hold at most 168 registers.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
 mla_tc_kernel(const __grid_constant__ MlaTcArgs A, Plan plan) {
+  griddep_launch_dependents();   // the next call's first kernel may start its launch
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);

@@ -67,6 +67,27 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Launch the first kernel of a public call as a programmatic dependent of
+// whatever kernel precedes it in the stream.  Such a kernel calls
+// griddep_wait() before its first memory access, so only its launch and CTA
+// set-up overlap the preceding kernel's tail, never its reads or writes (and
+// when the preceding work is not a kernel the launch is an ordinary one).
+template <typename... Exp, typename... Act>
+cudaError_t launch_chained(void (*kernel)(Exp...), unsigned grid, unsigned block, size_t smem,
+                           cudaStream_t st, Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

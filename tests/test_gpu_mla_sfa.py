@@ -379,3 +379,32 @@ def test_sfa_bad_slots_are_counted_and_masked(lib, hq):
             _, _, po_ref, pl_ref = exp[h]
             for r in range(cfg.dcp):
                 check(cfg, po[r, b, h], pl[r, b, h], po_ref[r], pl_ref[r], f"r{r} b{b} h{h}")
+
+
+# The fused call merges the per-rank partials inside the partials kernel (a
+# cluster of the request's CTAs); its output must be bitwise that of the
+# page-defined seam: dcp_sfa_decode_partial, then dcp_lse_merge with the sink.
+SFA_SEAM = [
+    SFA,                                                                   # clusters of 4
+    dataclasses.replace(SFA, B=40, lengths=[600 + 97 * i for i in range(40)], topk=128),  # of 3
+    dataclasses.replace(SFA, B=2, lengths=[60000, 9000], topk=2048),       # ranks one per CTA
+    dataclasses.replace(SFA, B=3, Hq=128, lengths=[20000, 4000, 1700], topk=1000, dcp=4),
+]
+
+
+@pytest.mark.parametrize("cfg", SFA_SEAM, ids=lambda c: f"B{c.B}-H{c.Hq}-dcp{c.dcp}-k{c.topk}")
+def test_sfa_fused_equals_partials_then_merge(lib, cfg):
+    wl = D.build(cfg)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for out_dtype in (torch.float32, torch.bfloat16):
+        out, lse = lib.sfa_decode(wl.layout, wl.q, wl.kv, wl.topk, wl.seq_lens, cfg.scale, cfg.dv,
+                                  sink=wl.sink, out_dtype=out_dtype, err=err)
+        rk, sl = lib.sfa_remap(wl.layout, wl.topk, wl.seq_lens, wl.block_table, wl.num_blocks,
+                               err=err)
+        po, pl = lib.sfa_decode_partial(wl.layout, wl.q, wl.kv, rk, sl, cfg.scale, cfg.dv, err=err)
+        mo, ml = lib.lse_merge(po, pl, wl.sink, out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        bits = torch.int32 if out_dtype == torch.float32 else torch.int16
+        assert torch.equal(out.view(bits), mo.view(bits)), "fused output differs from partials + merge"
+        assert torch.equal(lse.view(torch.int32), ml.view(torch.int32))
