@@ -209,6 +209,19 @@ def job_value(units_per_rank, world, seconds):
 # algorithmic bytes
 # ---------------------------------------------------------------------------
 
+def workload_config(cfg, lens, world):
+    """The workload a line measures (the same dict in both arms)."""
+    import numpy as np
+    kv = step_bytes(cfg, lens, len(lens))[0]
+    if cfg.kind == "sfa":
+        kv = cfg.B * cfg.topk * cfg.dk * 2
+    return {"workload": cfg.description, "name": cfg.name, "batch": cfg.B,
+            "context_tokens": int(np.asarray(lens, dtype=np.int64).sum()),
+            "kv_bytes_per_step": int(kv),
+            "parallelism": f"dcp{cfg.dcp} virtual ranks on 1 GPU" +
+                           (f" x {world} replicas" if world > 1 else "")}
+
+
 def step_bytes(cfg, lens, B):
     """(KV bytes, total algorithmic bytes) of one decode step."""
     import numpy as np
@@ -462,15 +475,12 @@ def measure(cfg, args, world, dev, local_rank, with_e2e=True):
         "unit": "GB/s",
         "ms_per_step": round(step_ms, 4),
         "decode_tok_per_s": round(job_value(B, world, step_ms * 1e-3), 1),
-        "config": {"workload": cfg.description, "name": cfg.name, "batch": B,
-                   "context_tokens": int(wl.seq_lens_host.astype("int64").sum()),
-                   "kv_bytes_per_step": kv_bytes, "l2": "inputs larger than L2 (KV >> 129 MB)"
-                   if not flush else "L2 flushed before every timed call (512 MB write)",
-                   "parallelism": f"dcp{cfg.dcp} virtual ranks on 1 GPU" +
-                                  (f" x {world} replicas" if world > 1 else ""),
+        "config": workload_config(cfg, wl.seq_lens_host, world),
+        "timing": {"l2": "inputs larger than L2 (KV >> 129 MB)" if not flush
+                   else "L2 flushed before every timed call (512 MB write)",
                    "launch": "step kernels launched one by one" if args.no_graph
-                             else "step replayed as one CUDA graph (e2e: the step and its "
-                                  "host copies replayed as one graph)"},
+                   else "step replayed as one CUDA graph (e2e: the step and its host copies "
+                        "replayed as one graph)"},
         "roofline": roof,
         "roofline_detail": {"kernel": f"dcp_decode_{cfg.kind} (plan + split + merge)",
                             "alg_bytes_per_launch": alg_bytes, "alg_flops_per_launch": flops,
@@ -524,6 +534,7 @@ def run_ours(args, rank, world, local_rank):
         "dtype": cfg.dtype,
         "data": "synthetic (seeded N(0,1) values; context lengths from the trace statistics)",
         "config": head["config"],
+        "timing": head["timing"],
         "decode_tok_per_s": head["decode_tok_per_s"],
         "e2e": head["e2e"],
         "roofline": head["roofline"],
@@ -543,8 +554,8 @@ def run_ours(args, rank, world, local_rank):
             extra[name] = {k: r[k] for k in ("value", "unit", "ms_per_step", "decode_tok_per_s",
                                              "roofline", "roofline_detail", "e2e", "clocks",
                                              "gpu_launches")}
-            extra[name]["workload"] = r["config"]["workload"]
-            extra[name]["l2"] = r["config"]["l2"]
+            extra[name]["config"] = r["config"]
+            extra[name]["timing"] = r["timing"]
         res["configs"] = extra
     return res, cfg, lens
 
@@ -679,7 +690,7 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * tot_s / max(1, args.steps), 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.description, "name": cfg.name},
+        "config": workload_config(cfg, lens, world),
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": blas_threads(),
                          "kind": "oracle", "cpu_model": cpu_model(), "nproc": os.cpu_count(),
                          "sample": f"per step: {what}",

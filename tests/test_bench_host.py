@@ -70,3 +70,16 @@ def test_cpu_baseline_reports_the_host_and_the_sample_share():
     assert cb["step_kv_bytes"] == bench.step_bytes(cfg, lens, cfg.B)[0]
     assert 0 < cb["sample_fraction_of_step"] <= 1.0
     assert cb["sample_kv_bytes"] == round(cb["sample_fraction_of_step"] * cb["step_kv_bytes"])
+
+
+def test_both_arms_name_the_same_workload():
+    import workloads as W
+    cfg = W.CONFIGS["gqa_bf16_b32"]
+    lens = W.make_seq_lens(cfg)
+    c = bench.workload_config(cfg, lens, 1)
+    assert c == bench.workload_config(cfg, lens.copy(), 1)
+    assert c["kv_bytes_per_step"] == bench.step_bytes(cfg, lens, cfg.B)[0]
+    assert set(c) == {"workload", "name", "batch", "context_tokens", "kv_bytes_per_step",
+                      "parallelism"}
+    sfa = W.CONFIGS["sfa_bf16_b32"]
+    assert bench.workload_config(sfa, W.make_seq_lens(sfa), 1)["kv_bytes_per_step"] == 32 * 2048 * 1152
