@@ -114,3 +114,22 @@ def test_gqa_bf16_b32_full_size_all_heads(lib):
 
 def test_longtail_gqa_full_size_all_heads(lib):
     full_check(lib, W.CONFIGS["longtail_gqa"])
+
+
+def test_sixteen_ranks(lib):
+    cfg = dataclasses.replace(BASE, B=3, lengths=[70000, 3000, 17], dcp=16, bs=16, I=1)
+    wl = D.build(cfg)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = lib.decode_gqa(wl.layout, wl.q, wl.kv, wl.local_lens, cfg.scale, err=err)
+    po, pl = lib.decode_partial_gqa(wl.layout, wl.q, wl.kv, wl.local_lens, cfg.scale, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    po, pl = po.cpu().numpy(), pl.cpu().numpy()
+    for b in range(cfg.B):
+        exp = ref.gqa_expected(cfg, wl.seq_lens_host, b, range(cfg.Hq))
+        for h in range(cfg.Hq):
+            o_ref, lse_ref, po_ref, pl_ref = exp[h]
+            ref.check_bf16(out[b, h], lse[b, h], o_ref, lse_ref, f"b{b} h{h}")
+            for r in range(cfg.dcp):
+                ref.check_bf16(po[r, b, h], pl[r, b, h], po_ref[r], pl_ref[r], f"r{r} b{b} h{h}")

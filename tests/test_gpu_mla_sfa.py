@@ -408,3 +408,45 @@ def test_sfa_fused_equals_partials_then_merge(lib, cfg):
         bits = torch.int32 if out_dtype == torch.float32 else torch.int16
         assert torch.equal(out.view(bits), mo.view(bits)), "fused output differs from partials + merge"
         assert torch.equal(lse.view(torch.int32), ml.view(torch.int32))
+
+
+# 16 ranks: one rank per CTA gives groups of 16, above the portable cluster
+# size, so the fused call keeps the separate merge kernel; the partials and
+# the merged output still match the oracle
+def test_sfa_sixteen_ranks_separate_merge(lib):
+    cfg = dataclasses.replace(SFA, B=2, lengths=[40000, 9000], topk=512, dcp=16)
+    wl = D.build(cfg)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = lib.sfa_decode(wl.layout, wl.q, wl.kv, wl.topk, wl.seq_lens, cfg.scale, cfg.dv,
+                              sink=wl.sink, out_dtype=torch.float32, err=err)
+    rk, sl = lib.sfa_remap(wl.layout, wl.topk, wl.seq_lens, wl.block_table, wl.num_blocks, err=err)
+    po, pl = lib.sfa_decode_partial(wl.layout, wl.q, wl.kv, rk, sl, cfg.scale, cfg.dv, err=err)
+    mo, ml = lib.lse_merge(po, pl, wl.sink)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(out.view(torch.int32), mo.view(torch.int32))
+    out, lse, po, pl = (t.cpu().numpy() for t in (out, lse, po, pl))
+    sink = wl.sink.cpu().numpy()
+    for b in range(cfg.B):
+        heads = [0, 21, 63]
+        exp = ref.sfa_expected(cfg, wl.seq_lens_host, wl.topk_host, b, heads, sink=sink)
+        for h in heads:
+            o_ref, lse_ref, po_ref, pl_ref = exp[h]
+            check(cfg, out[b, h], lse[b, h], o_ref, lse_ref, f"fused b{b} h{h}")
+            for r in range(cfg.dcp):
+                check(cfg, po[r, b, h], pl[r, b, h], po_ref[r], pl_ref[r], f"r{r} b{b} h{h}")
+
+
+def test_mla_sixteen_ranks(lib):
+    cfg = dataclasses.replace(MLA, B=2, lengths=[30000, 5000], dcp=16, bs=64, I=1)
+    wl = D.build(cfg)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = lib.decode_mla(wl.layout, wl.q, wl.kv, wl.local_lens, cfg.scale, cfg.dv,
+                              out_dtype=torch.float32, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    for b in range(cfg.B):
+        exp = ref.mla_expected(cfg, wl.seq_lens_host, b, [0, 64, 127])
+        for h in (0, 64, 127):
+            check(cfg, out[b, h], lse[b, h], exp[h][0], exp[h][1], f"b{b} h{h}")
