@@ -35,12 +35,13 @@
 //    softmax's maximum and sum need no exchange between threads;
 //  * four warps gather with 16-byte cp.async (whole 1152-byte rows;
 //    unselected, unusable and tail rows are zero-filled).  Each walks every
-//    stage, taking a quarter of its rows, and
-//    never waits for its copies: cp.async.mbarrier.arrive.noinc arrives on
-//    the slot's barrier once the thread's copies have landed, so all five
-//    warps start on a slot the moment it is free.  The threads that wait on
-//    that barrier fence the data for the tensor core;
-//  * one thread issues a tcgen05.mma only every ~55-80 cycles, so Q.K^T is
+//    stage, taking a quarter of its rows, and never waits for its copies:
+//    cp.async.mbarrier.arrive.noinc arrives on the slot's barrier once the
+//    thread's copies have landed, so all four warps start on a slot the
+//    moment it is free.  The threads that wait on that barrier fence the
+//    data for the tensor core.  The rows carry an L2 evict-first hint and
+//    the partials an evict-last hint, so the merge finds the partials in L2;
+//  * one thread issues a tcgen05.mma only every ~55-100 cycles, so Q.K^T is
 //    split between two issuing warps (latent chunks 0-4 and 5-8) into two
 //    partial accumulators that the softmax adds, in a fixed order, and P V
 //    between two more (O^T value rows 0-255 and 256-511);
@@ -48,16 +49,17 @@
 //    (4 x 64 columns);
 //  * in the fused decode the CTAs of a (request, head block) form a cluster:
 //    once each has written its ranks' partials (and a cluster barrier made
-//    them visible), each merges its share of the request's (head, 128-value
-//    chunk) rows by LSE from L2, with the sink applied once, so no separate
-//    merge launch waits for the whole grid;
+//    them visible), each merges its share of the request's head rows by LSE
+//    from L2 (one warp per row, every part loaded before any is used), with
+//    the sink applied once, so no separate merge launch waits for the whole
+//    grid;
 //  * warps 0-3: softmax of their lane quarter's 16 heads (threads l and
 //    l + 16 take tokens 0-31 and 32-63 of head 16 q + l), rescale and
 //    epilogue of their quarter of O^T (value rows).  Warps 4 and 6 issue
 //    Q.K^T, warps 5 and 7 P V.  O^T columns (heads) are rescaled
 //    only when a head's running maximum grows by more than 8 (log2 units),
-//    which keeps P <= 256; the P V warp orders that rescale between two
-//    P Vs.
+//    which keeps P <= 256; the leading P V warp orders that rescale between
+//    two P Vs.
 // Every mbarrier wait is bounded; a timed-out wait adds 1<<20 to the error
 // counter and that role stops waiting, so the kernel always terminates.
 #include <stdlib.h>
