@@ -522,25 +522,18 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
         break;
       }
       tc_fence_after();
-      // S = S_a + S_b for tokens 0-31 (kept) and 32-63 (handed to lane + 16);
-      // lanes 16-31 of the quarter hold no head (M=64 layout)
+      // S = S_a + S_b: head hl's row sits in tensor-memory lane hl % 16 of
+      // the quarter (M=64 layout); the 16x32bx2 load gives thread l its
+      // tokens 0-31 and thread l + 16 its tokens 32-63
       float s[32];
       {
-        uint32_t a0[32], b0[32], a1[32], b1[32];
-        tc_ld32(tmem + lane_off + kColSa + sb * kSt, a0);
-        tc_ld32(tmem + lane_off + kColSb + sb * kSt, b0);
-        tc_ld32(tmem + lane_off + kColSa + sb * kSt + 32, a1);
-        tc_ld32(tmem + lane_off + kColSb + sb * kSt + 32, b1);
-        tc_wait_ld(a0);
-        tc_wait_ld(b0);
-        tc_wait_ld(a1);
-        tc_wait_ld(b1);
+        uint32_t a[32], c[32];
+        tc_ld16x2_32<32>(tmem + lane_off + kColSa + sb * kSt, a);
+        tc_ld16x2_32<32>(tmem + lane_off + kColSb + sb * kSt, c);
+        tc_wait_ld(a);
+        tc_wait_ld(c);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float up = __shfl_sync(0xffffffffu, __uint_as_float(a1[i]) + __uint_as_float(b1[i]),
-                                       lane & 15);
-          s[i] = hi ? up : __uint_as_float(a0[i]) + __uint_as_float(b0[i]);
-        }
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(a[i]) + __uint_as_float(c[i]);
       }
       tc_fence_before();
       // tokens of the stage that are attended: lane t checks tokens t, t + 32
@@ -550,10 +543,12 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
       const uint32_t v_hi =
           __ballot_sync(0xffffffffu, lane + 32 < cnt && sel[s0 + lane + 32] >= 0);
       const uint32_t vm = hi ? v_hi : v_lo;
-      // this head's stage maximum (raw scores; the scale is positive)
-      float mx = -INFINITY;
+      // this head's stage maximum (raw scores; the scale is positive), in
+      // four independent chains
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int t = 0; t < 32; ++t) mx = fmaxf(mx, ((vm >> t) & 1u) ? s[t] : -INFINITY);
+      for (int t = 0; t < 32; ++t) mq[t & 3] = fmaxf(mq[t & 3], ((vm >> t) & 1u) ? s[t] : -INFINITY);
+      float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       const float tm = mx * A.sl2;
       const bool grow = tm > m2 + kRescaleThreshold;
@@ -566,13 +561,13 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
       if (lane == 0) flags[sb * 4 + warp] = need_w != 0 ? 1 : 0;
       // P (fp32 in s) and this thread's half of row hl of P^T in the slot's
       // rope chunk: 32 tokens (bf16), 16-byte units swizzled by hl & 7
-      float ps = 0.f;
+      float pq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int t = 0; t < 32; ++t) {
         s[t] = ((vm >> t) & 1u) ? ex2_ftz(fmaf(s[t], A.sl2, -m2)) : 0.f;
-        ps += s[t];
+        pq[t & 3] += s[t];
       }
-      l2 += ps;
+      l2 += (pq[0] + pq[1]) + (pq[2] + pq[3]);
       {
         const uint32_t prow = sbase + kSlotOff + sb * kStageB + 8 * kChunkB + hl * 128;
         const int u0 = hi ? 4 : 0;
