@@ -337,8 +337,8 @@ __global__ void __launch_bounds__(kSfaTcThreads, 1) sfa_tc_kernel(const __grid_c
       // group); each copy instruction moves chunk c of the 4 rows: lane l
       // copies 16-byte unit l % 8 of row 4 g + l / 8, swizzled by the row & 7.
       // All 32 lanes copy in every instruction: the load pipe's cost is per
-      // instruction, whatever its active lanes.  16 groups over five warps:
-      // the warp with the sixteenth group changes from stage to stage.
+      // instruction, whatever its active lanes.  16 groups over four warps,
+      // four each, which groups rotating from stage to stage.
       const int rsub = lane >> 3, un = lane & 7;
 #pragma unroll 1
       for (int rg = (gw + n) % kGatherWarps; rg < kSt / 4; rg += kGatherWarps) {

@@ -381,6 +381,48 @@ def test_sfa_bad_slots_are_counted_and_masked(lib, hq):
                 check(cfg, po[r, b, h], pl[r, b, h], po_ref[r], pl_ref[r], f"r{r} b{b} h{h}")
 
 
+@pytest.mark.parametrize("hq", [64, 128])
+def test_sfa_fused_bad_block_table_entries_are_counted_and_dropped(lib, hq):
+    """A selected token whose block-table entry is unusable is dropped by the
+    fused call and counted once, as dcp_sfa_remap drops and counts it for the
+    same table, and the output equals the oracle's with those entries
+    dropped."""
+    import context_paged_decode_gb300 as dcp
+    cfg = dataclasses.replace(SFA, B=2, Hq=hq, lengths=[5000, 900], topk=256, dcp=4, bs=64, I=1)
+    wl = D.build(cfg)
+    topk = wl.topk_host.copy()
+    vbs = cfg.bs * cfg.dcp
+    bt = wl.block_table.clone()
+    rk_good, _ = lib.sfa_remap(wl.layout, wl.topk, wl.seq_lens, wl.block_table, wl.num_blocks)
+    rk_good = rk_good.cpu().numpy()
+    # unusable entries of three (rank, request, virtual block) that selected
+    # tokens go through: past the pool, negative, and past the pool again
+    picks = [(0, 3, wl.num_blocks + 5), (0, 100, -3), (1, 7, wl.num_blocks)]
+    for b, k, val in picks:
+        assert rk_good[b, k] >= 0
+        bt[rk_good[b, k], b, int(topk[b, k]) // vbs] = val
+    kv = dcp.PagedKV(wl.kv.k_pools, None, bt, wl.num_blocks)
+    err_remap = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rk_bad, _ = lib.sfa_remap(wl.layout, wl.topk, wl.seq_lens, bt, wl.num_blocks, err=err_remap)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = lib.sfa_decode(wl.layout, wl.q, kv, wl.topk, wl.seq_lens, cfg.scale, cfg.dv,
+                              sink=wl.sink, out_dtype=torch.float32, err=err)
+    torch.cuda.synchronize()
+    rk_bad = rk_bad.cpu().numpy()
+    dropped = (rk_bad < 0) & (rk_good >= 0)
+    assert dropped.sum() >= len(picks)
+    assert err_remap.item() == dropped.sum()
+    assert err.item() == err_remap.item()
+    topk[dropped] = -1                                    # the oracle drops them
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    sink = None if wl.sink is None else wl.sink.cpu().numpy()
+    for b in range(cfg.B):
+        heads = [0, 37, hq - 1]
+        exp = ref.sfa_expected(cfg, wl.seq_lens_host, topk, b, heads, sink=sink)
+        for h in heads:
+            check(cfg, out[b, h], lse[b, h], exp[h][0], exp[h][1], f"b{b} h{h}")
+
+
 # The fused call merges the per-rank partials inside the partials kernel (a
 # cluster of the request's CTAs); its output must be bitwise that of the
 # page-defined seam: dcp_sfa_decode_partial, then dcp_lse_merge with the sink.
