@@ -69,7 +69,7 @@ NCU_TRAFFIC = {
                      "kv_bytes": 216885 * 1152,
                      "capture": "profiles/mla_tc_kernel_mla_bf16_b64.md"},
     "sfa_bf16_b32": {"source": "context_paged_decode_gb300/csrc/dcp_sfa_tc.cu",
-                     "sha256_16": "952d2b63395947a4", "dram_bytes": 78462720 + 2963456,
+                     "sha256_16": "14ff0928b47b9535", "dram_bytes": 78460672 + 2981376,
                      "kv_bytes": 32 * 2048 * 1152,
                      "capture": "profiles/sfa_tc_kernel_sfa_bf16_b32.md"},
 }
