@@ -61,11 +61,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernel source is the one captured (sha256 prefix); otherwise null.
 NCU_TRAFFIC = {
     "gqa_bf16_b32": {"source": "context_paged_decode_gb300/csrc/dcp_gqa.cu",
-                     "sha256_16": "a123735c3fb9abc0", "dram_bytes": 1159452000 + 7022592,
+                     "sha256_16": "e99da6e59345a4eb", "dram_bytes": 1159464704 + 6609152,
                      "kv_bytes": 282732 * 4096,
                      "capture": "profiles/gqa_tma_kernel_gqa_bf16_b32.md"},
     "mla_bf16_b64": {"source": "context_paged_decode_gb300/csrc/dcp_mla_tc.cu",
-                     "sha256_16": "4bca62db4a1b2bdf", "dram_bytes": 251376128 + 5723904,
+                     "sha256_16": "3fdb673daa322567", "dram_bytes": 251370240 + 5882112,
                      "kv_bytes": 216885 * 1152,
                      "capture": "profiles/mla_tc_kernel_mla_bf16_b64.md"},
     "sfa_bf16_b32": {"source": "context_paged_decode_gb300/csrc/dcp_sfa_tc.cu",
