@@ -41,7 +41,9 @@ def test_mla_small(lib, cfg):
                               out_dtype=torch.float32, err=err)
     po, pl, out, lse = (t.cpu().numpy() for t in (po, pl, out, lse))
     assert err.item() == 0
-    heads = range(cfg.Hq) if cfg.Hq <= 16 else [0, 1, 63, 64, 127]
+    # every head when the contexts are tiny (the full tiny MLA case: B=2,
+    # L={100, 37}, all 128 heads), else both ends of each half of the heads
+    heads = range(cfg.Hq) if cfg.Hq <= 16 or sum(cfg.lengths) <= 256 else [0, 1, 63, 64, 127]
     for b in range(cfg.B):
         exp = ref.mla_expected(cfg, wl.seq_lens_host, b, heads)
         for h in heads:
