@@ -25,6 +25,9 @@ SMALL = [
     dataclasses.replace(BASE, B=2, Hq=8, Hkv=8, lengths=[100, 1], dcp=2, bs=16, I=1),
     dataclasses.replace(BASE, B=2, Hq=8, Hkv=2, dk=64, dv=64, lengths=[100, 900], dcp=2, bs=16),
     dataclasses.replace(BASE, B=2, lengths=[40, 333], dcp=2, bs=8, I=2),
+    # a request with an empty context: output 0, LSE -inf (the sink's logit with a sink)
+    dataclasses.replace(BASE, B=3, lengths=[0, 100, 37], dcp=2, bs=16, I=1),
+    dataclasses.replace(W.CONFIGS["tiny_gqa_f32"], B=2, lengths=[37, 0]),
 ]
 
 

@@ -20,6 +20,8 @@ MLA_SMALL = [
     dataclasses.replace(MLA, B=2, lengths=[777, 64], dcp=3, bs=64, I=16),
     dataclasses.replace(MLA, B=2, Hq=16, lengths=[300, 5], dcp=2, bs=16, I=1),
     dataclasses.replace(MLA, B=2, Hq=4, dtype="f32", lengths=[90, 7], dcp=2, bs=16, I=2),
+    # a request with an empty context: output 0, LSE -inf
+    dataclasses.replace(MLA, B=3, lengths=[0, 300, 65], dcp=2, bs=64, I=1),
 ]
 
 
