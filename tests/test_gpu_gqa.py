@@ -28,6 +28,8 @@ SMALL = [
     # a request with an empty context: output 0, LSE -inf (the sink's logit with a sink)
     dataclasses.replace(BASE, B=3, lengths=[0, 100, 37], dcp=2, bs=16, I=1),
     dataclasses.replace(W.CONFIGS["tiny_gqa_f32"], B=2, lengths=[37, 0]),
+    # one rank: plain paged attention
+    dataclasses.replace(BASE, B=2, lengths=[500, 33], dcp=1, bs=16, I=1),
 ]
 
 

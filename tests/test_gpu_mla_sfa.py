@@ -22,6 +22,8 @@ MLA_SMALL = [
     dataclasses.replace(MLA, B=2, Hq=4, dtype="f32", lengths=[90, 7], dcp=2, bs=16, I=2),
     # a request with an empty context: output 0, LSE -inf
     dataclasses.replace(MLA, B=3, lengths=[0, 300, 65], dcp=2, bs=64, I=1),
+    # one rank: plain paged attention
+    dataclasses.replace(MLA, B=2, lengths=[200, 64], dcp=1, bs=64, I=1),
 ]
 
 
@@ -62,6 +64,8 @@ SFA_SMALL = [
                         I=16),
     dataclasses.replace(SFA, B=2, Hq=128, lengths=[9000, 300], topk=200, dcp=4, bs=64, I=64),
     dataclasses.replace(SFA, B=3, Hq=16, lengths=[3000, 17, 640], topk=16, dcp=2, bs=16, I=4),
+    # one rank: plain sparse attention
+    dataclasses.replace(SFA, B=2, lengths=[3000, 200], topk=128, dcp=1, bs=64, I=64),
 ]
 
 
