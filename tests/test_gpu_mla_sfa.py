@@ -66,6 +66,8 @@ SFA_SMALL = [
     dataclasses.replace(SFA, B=3, Hq=16, lengths=[3000, 17, 640], topk=16, dcp=2, bs=16, I=4),
     # one rank: plain sparse attention
     dataclasses.replace(SFA, B=2, lengths=[3000, 200], topk=128, dcp=1, bs=64, I=64),
+    # six ranks (the fused call merges in clusters of six)
+    dataclasses.replace(SFA, B=2, lengths=[9000, 1100], topk=300, dcp=6, bs=64, I=16),
 ]
 
 
@@ -439,6 +441,9 @@ SFA_SEAM = [
     dataclasses.replace(SFA, B=40, lengths=[600 + 97 * i for i in range(40)], topk=128),  # of 3
     dataclasses.replace(SFA, B=2, lengths=[60000, 9000], topk=2048),       # ranks one per CTA
     dataclasses.replace(SFA, B=3, Hq=128, lengths=[20000, 4000, 1700], topk=1000, dcp=4),
+    # clusters of 6 and 7 CTAs (one rank each)
+    dataclasses.replace(SFA, B=3, lengths=[30000, 7000, 2500], topk=700, dcp=6, bs=64, I=16),
+    dataclasses.replace(SFA, B=2, lengths=[40000, 3000], topk=1500, dcp=7, bs=64, I=8),
 ]
 
 
