@@ -68,6 +68,8 @@ SFA_SMALL = [
     dataclasses.replace(SFA, B=2, lengths=[3000, 200], topk=128, dcp=1, bs=64, I=64),
     # six ranks (the fused call merges in clusters of six)
     dataclasses.replace(SFA, B=2, lengths=[9000, 1100], topk=300, dcp=6, bs=64, I=16),
+    # more selected tokens than the tcgen05 kernel lists (2048): the other path
+    dataclasses.replace(SFA, B=2, lengths=[20000, 5000], topk=3000, dcp=4, bs=64, I=64),
 ]
 
 
